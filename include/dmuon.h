@@ -1,0 +1,178 @@
+/*
+ * dmuon.h -- C ABI of the GB300 owner-rank Muon update library (libdmuon.so).
+ *
+ * The library runs, on one GPU, the per-parameter Muon update that a DMuon owner rank performs on
+ * the matrices it owns: momentum accumulate, fp32 Frobenius normalisation, five-step fp16
+ * Newton-Schulz (direct or Gram form) and the weight update.
+ *
+ * Sources (DMuon documentation and a blog post on distributed Muon):
+ *   - "Newton-Schulz 变体" (Newton-Schulz variants) page: sections "直接空间 NS（经典）" (direct
+ *     iteration), "Gram 空间 NS（Dao-AILab）" (Gram iteration), "精度流水线" (fp32 normalisation, fp16
+ *     iteration), "系数集" (coefficient tables), "重启机制" (restarts), "使用自定义系数集" (the
+ *     newton_schulz / NewtonSchulz / Muon calls these entry points stand for).
+ *   - DMuon "Core Concepts" page, section "1. Dedicated Ownership": the owner runs Newton-Schulz on
+ *     the full matrix with no extra communication.
+ *   - pwwt.cn blog on distributed Muon, section "2. Muon执行过程": momentum, then orthogonalise it.
+ *
+ * Conventions for every entry point:
+ *   - Pointers named "device" must be CUDA device (or managed) memory on the current device;
+ *     "host" pointers are read during the call only and may be freed when it returns.
+ *   - Matrices are dense row-major with the given rows x cols and no padding. Device buffers
+ *     passed to the library must be 16-byte aligned.
+ *   - The caller owns all tensors. The library owns a cached workspace per device (grown on first
+ *     use for a set of shapes, kept until dmuon_release_workspace) and descriptor tables. Calls that
+ *     share a device must be serialised by the caller (same stream, or synchronised streams).
+ *   - Work is enqueued on `cuda_stream` (a cudaStream_t; NULL = legacy default stream); the call
+ *     returns before the GPU finishes. No host synchronisation happens except when a new shape set
+ *     needs workspace or new descriptors (first call).
+ *   - Every function returns a dmuon_status. Arguments are validated before anything is
+ *     launched; on an invalid argument nothing is launched and dmuon_last_error() says why.
+ *     Errors the GPU detects while running (a bounded wait that gave up, a non-finite fp16 value)
+ *     are recorded in a device status word read by dmuon_check_status().
+ */
+#ifndef DMUON_H
+#define DMUON_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define DMUON_API __attribute__((visibility("default")))
+#else
+#define DMUON_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum dmuon_status {
+  DMUON_OK = 0,
+  DMUON_ERR_INVALID_ARG = 1, /* bad pointer, size, enum, restart list or alignment            */
+  DMUON_ERR_UNSUPPORTED = 2, /* no sm_103a device, or a shape beyond the library's limits        */
+  DMUON_ERR_OOM = 3,         /* workspace allocation failed or exceeds the set limit           */
+  DMUON_ERR_CUDA = 4,        /* a CUDA runtime/driver call failed (text in dmuon_last_error)  */
+  DMUON_ERR_TIMEOUT = 5,     /* a device-side bounded wait gave up (reported by check_status)  */
+  DMUON_ERR_NONFINITE = 6    /* an fp16 intermediate overflowed or became NaN (check_status)   */
+} dmuon_status;
+
+typedef enum dmuon_ns_backend {
+  DMUON_NS_DIRECT = 0, /* X <- a X + b (X X^T) X + c (X X^T)^2 X                                 */
+  DMUON_NS_GRAM = 1    /* R = X X^T, Z = b R + c R^2, Q <- Z Q + a Q, R <- (aI+Z) R (aI+Z), Q X   */
+} dmuon_ns_backend;
+
+typedef enum dmuon_dtype { DMUON_F32 = 0, DMUON_BF16 = 1 } dmuon_dtype;
+
+/* Largest number of Newton-Schulz steps accepted (coefficient triples per call). */
+#define DMUON_MAX_STEPS 16
+
+/*
+ * dmuon_ns -- Newton-Schulz orthogonalisation of one matrix, in place.
+ *   ("Newton-Schulz 变体": newton_schulz(G, coefficients=..., restart_iterations=[...]) /
+ *    NewtonSchulz(backend, ...); precision pipeline of section "精度流水线".)
+ *
+ *   x          device fp32, rows m x cols n. Input G; on return O = NS(G / (||G||_F + eps)) in the same
+ *              orientation. Internally a matrix with m > n is worked on as its transpose (m x m Gram
+ *              matrices stay the small ones) and written back transposed.
+ *   coeffs     host, 3 * steps floats (a_0, b_0, c_0, a_1, ...): one odd polynomial per step.
+ *   steps      1 .. DMUON_MAX_STEPS.
+ *   restarts   host, n_restarts ints, strictly increasing, each in [0, steps - 1]; a restart at k
+ *              happens before step k (Gram backend only; ignored by the direct backend). May be NULL
+ *              when n_restarts == 0. Index 0 is accepted and has no effect.
+ *   backend    DMUON_NS_DIRECT or DMUON_NS_GRAM.
+ *   eps        added to the Frobenius norm (not to its square); must be >= 0.
+ * Intermediates are fp16 with fp32 accumulation. A zero matrix gives a zero output.
+ */
+DMUON_API int dmuon_ns(float* x, int64_t m, int64_t n, const float* coeffs, int steps, const int* restarts,
+             int n_restarts, int backend, float eps, void* cuda_stream);
+
+/*
+ * dmuon_muon_step -- one owner-rank Muon update over `count` matrices, batched.
+ *   (DMuon "Core Concepts", step "Owner NS update"; Muon(model, lr, ns_backend) on the
+ *    "Newton-Schulz 变体" page; momentum-then-orthogonalise of the pwwt.cn post, section 2.)
+ *
+ * For each matrix i (rows[i] x cols[i], row-major):
+ *   M_i <- beta * M_i + G_i                                  (fp32, in place)
+ *   X_i  = fp16(M_i / (||M_i||_F + eps)), transposed if rows > cols
+ *   O_i  = NS(X_i) with `backend`, `coeffs`, `restarts`       (fp16 operands, fp32 accumulation)
+ *   W_i <- W_i - lr * O_i                                     (fp32, in place, original orientation)
+ * All matrices advance phase by phase; each phase is one grouped GPU launch over all of them.
+ *
+ *   count      number of matrices, >= 1.
+ *   params     host array of `count` device fp32 pointers W_i.
+ *   grads      host array of `count` device pointers G_i, element type `grad_dtype` (fp32 or bf16).
+ *   momenta    host array of `count` device fp32 pointers M_i (the momentum state; zero to start).
+ *   rows, cols host arrays of `count` sizes, each >= 1.
+ *   norms_out  device fp32 array of `count` entries receiving ||M_i||_F after the momentum update,
+ *              or NULL.
+ *   lr, beta, coeffs, steps, restarts, n_restarts, backend, eps: as above / dmuon_ns.
+ * W_i, G_i and M_i must not overlap one another or another matrix's buffers.
+ */
+DMUON_API int dmuon_muon_step(int count, float* const* params, const void* const* grads, int grad_dtype,
+                    float* const* momenta, const int64_t* rows, const int64_t* cols,
+                    float* norms_out, float lr, float beta, const float* coeffs, int steps,
+                    const int* restarts, int n_restarts, int backend, float eps, void* cuda_stream);
+
+/*
+ * dmuon_momentum_normalize -- the first half of dmuon_muon_step on its own ("精度流水线", stage 1,
+ * preceded by the momentum accumulate): for each matrix
+ *   M_i <- beta * M_i + G_i (skipped when grads == NULL: M_i is then only read),
+ *   norms_out[i] = ||M_i||_F,  X_i = fp16(M_i / (||M_i||_F + eps)) in the m <= n orientation.
+ *
+ *   x_out      host array of `count` device pointers to caller-owned fp16 buffers of
+ *              min(rows,cols) x max(rows,cols) elements, row-major (the oriented X_i).
+ *   norms_out  device fp32 array of `count` entries (required here).
+ * Other arguments as in dmuon_muon_step.
+ */
+DMUON_API int dmuon_momentum_normalize(int count, const void* const* grads, int grad_dtype,
+                             float* const* momenta, const int64_t* rows, const int64_t* cols,
+                             void* const* x_out, float* norms_out, float beta, float eps,
+                             void* cuda_stream);
+
+/*
+ * dmuon_gemm_f16 -- the tensor-core building block of both iterations, exposed for testing and for
+ * callers composing their own schedules. With A (M x K, fp16, row-major, lda), B (fp16, ldb) and
+ * an optional E (M x N, fp16, lde):
+ *   acc[i][j] = sum_k A[i][k] * Bop[k][j],  Bop = B^T when b_trans != 0 (B is N x K; e.g. X X^T),
+ *                                           Bop = B    when b_trans == 0 (B is K x N; e.g. Q X)
+ *   v[i][j]   = alpha * acc[i][j] + beta * E[i][j] + (i == j ? gamma : 0)     (fp32)
+ *   D[i][j]   = fp16(v[i][j])   (D: M x N fp16, ldd)
+ * symmetric != 0 requires M == N and computes only tiles touching the upper triangle, writing
+ * D[i][j] and D[j][i] from the upper-triangle value (the SYRK form of X X^T and R^2).
+ * E may be NULL (beta is then ignored). Leading dimensions are in elements, >= the row length,
+ * and must make every row start 16-byte aligned (multiples of 8). A, B, E and D must not overlap.
+ */
+DMUON_API int dmuon_gemm_f16(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
+                   int64_t ldb, int b_trans, const void* E, int64_t lde, void* D, int64_t ldd,
+                   float alpha, float beta, float gamma, int symmetric, void* cuda_stream);
+
+/*
+ * dmuon_check_status -- synchronise `cuda_stream`, then read and clear the device status word.
+ * Returns DMUON_OK, DMUON_ERR_TIMEOUT (a kernel's bounded wait gave up: its results are invalid),
+ * DMUON_ERR_NONFINITE (an fp16 intermediate overflowed or was NaN) or DMUON_ERR_CUDA (an
+ * asynchronous CUDA error surfaced during synchronisation).
+ */
+DMUON_API int dmuon_check_status(void* cuda_stream);
+
+/* Text of the last error on the calling thread; valid until the next call on that thread. */
+DMUON_API const char* dmuon_last_error(void);
+
+/* Library version string, e.g. "dmuon-gb300 0.1.0 (sm_103a)". */
+DMUON_API const char* dmuon_version(void);
+
+/* Upper bound on workspace bytes per device (0 = no limit). Calls needing more fail with
+ * DMUON_ERR_OOM before launching anything. */
+DMUON_API int dmuon_set_workspace_limit(size_t bytes);
+
+/* Bytes of workspace the library would need for dmuon_muon_step on these shapes (host query). */
+DMUON_API int dmuon_workspace_size(int count, const int64_t* rows, const int64_t* cols, int backend,
+                         size_t* bytes_out);
+
+/* Synchronise the current device and free its workspace and cached descriptor tables. */
+DMUON_API int dmuon_release_workspace(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DMUON_H */

@@ -1,0 +1,249 @@
+"""Thin Python binding of libdmuon (the C ABI in include/dmuon.h): argument marshalling only.
+
+Every step of the update runs in the CUDA library; this module passes device pointers, sizes and the
+current CUDA stream through ctypes. There is no CPU fallback: if libdmuon.so has not been built, every
+call raises ``LibraryNotBuilt``.
+
+    import newton_schulz_momentum_gb300 as dm
+    dm.ns(x, dm.POLAR_EXPRESS, restarts=(2,), backend="gram")          # in place, fp32 CUDA tensor
+    dm.muon_step(params, grads, momenta, lr=0.02, beta=0.95, coeffs=dm.POLAR_EXPRESS)
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Sequence
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libdmuon.so")
+
+# Coefficient tables printed on the DMuon "Newton-Schulz 变体" page, section "系数集".
+POLAR_EXPRESS = (
+    (7.893, -20.381, 14.939),
+    (3.912, -2.544, 0.470),
+    (3.761, -2.512, 0.476),
+    (3.160, -2.148, 0.440),
+    (2.191, -1.441, 0.361),
+)
+YOU = (
+    (4.0848, -6.8946, 2.9270),
+    (3.9505, -6.3029, 2.6377),
+    (3.7418, -5.5913, 2.3037),
+    (2.8769, -3.1427, 1.2046),
+    (2.8366, -3.0525, 1.2012),
+)
+DEFAULT_RESTARTS = (2,)
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_OOM, ERR_CUDA, ERR_TIMEOUT, ERR_NONFINITE = range(7)
+_STATUS_NAMES = {1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "OOM", 4: "CUDA", 5: "TIMEOUT", 6: "NONFINITE"}
+BACKENDS = {"direct": 0, "gram": 1}
+F32, BF16 = 0, 1
+
+EXPORTS = (
+    "dmuon_ns", "dmuon_muon_step", "dmuon_momentum_normalize", "dmuon_gemm_f16", "dmuon_check_status",
+    "dmuon_last_error", "dmuon_version", "dmuon_set_workspace_limit", "dmuon_workspace_size",
+    "dmuon_release_workspace",
+)
+
+
+class LibraryNotBuilt(RuntimeError):
+    pass
+
+
+class DmuonError(RuntimeError):
+    def __init__(self, status, message):
+        super().__init__(f"dmuon error {_STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+_lib = None
+
+_c_i64p = ctypes.POINTER(ctypes.c_int64)
+_c_vpp = ctypes.POINTER(ctypes.c_void_p)
+_c_fp = ctypes.POINTER(ctypes.c_float)
+_c_ip = ctypes.POINTER(ctypes.c_int)
+
+
+def lib():
+    """Load libdmuon.so (once). Raises LibraryNotBuilt when it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise LibraryNotBuilt(f"{LIB_PATH} is missing; build it with newton_schulz_momentum_gb300.build.build()")
+    L = ctypes.CDLL(LIB_PATH)
+    vp, i64, i32, f32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float
+    L.dmuon_ns.argtypes = [vp, i64, i64, _c_fp, i32, _c_ip, i32, i32, f32, vp]
+    L.dmuon_muon_step.argtypes = [i32, _c_vpp, _c_vpp, i32, _c_vpp, _c_i64p, _c_i64p, vp, f32, f32, _c_fp, i32,
+                                  _c_ip, i32, i32, f32, vp]
+    L.dmuon_momentum_normalize.argtypes = [i32, _c_vpp, i32, _c_vpp, _c_i64p, _c_i64p, _c_vpp, vp, f32, f32, vp]
+    L.dmuon_gemm_f16.argtypes = [i64, i64, i64, vp, i64, vp, i64, i32, vp, i64, vp, i64, f32, f32, f32, i32, vp]
+    L.dmuon_check_status.argtypes = [vp]
+    L.dmuon_last_error.restype = ctypes.c_char_p
+    L.dmuon_version.restype = ctypes.c_char_p
+    L.dmuon_set_workspace_limit.argtypes = [ctypes.c_size_t]
+    L.dmuon_workspace_size.argtypes = [i32, _c_i64p, _c_i64p, i32, ctypes.POINTER(ctypes.c_size_t)]
+    for name in EXPORTS:
+        if name not in ("dmuon_last_error", "dmuon_version"):
+            getattr(L, name).restype = ctypes.c_int
+    _lib = L
+    return L
+
+
+def _check(status):
+    if status != OK:
+        raise DmuonError(status, lib().dmuon_last_error().decode(errors="replace"))
+
+
+def _ptr(t):
+    """Device address of a torch tensor (or an int address, or None)."""
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is not None:
+        return stream if isinstance(stream, int) else stream.cuda_stream
+    import torch
+    return torch.cuda.current_stream().cuda_stream
+
+
+def _coeff_array(coeffs):
+    flat = [float(v) for triple in coeffs for v in triple]
+    if len(flat) % 3 or not flat:
+        raise ValueError("coeffs must be a non-empty sequence of (a, b, c) triples")
+    return (ctypes.c_float * len(flat))(*flat), len(flat) // 3
+
+
+def _int_array(vals):
+    vals = [int(v) for v in vals]
+    return (ctypes.c_int * max(len(vals), 1))(*vals), len(vals)
+
+
+def _backend(backend):
+    if isinstance(backend, int):
+        return backend
+    return BACKENDS[backend]
+
+
+def version():
+    return lib().dmuon_version().decode()
+
+
+def ns(x, coeffs=POLAR_EXPRESS, restarts=DEFAULT_RESTARTS, backend="gram", eps=1e-7, stream=None):
+    """In-place Newton-Schulz of one fp32 CUDA matrix x (rows x cols, contiguous). Returns x."""
+    if x.dim() != 2 or not x.is_contiguous():
+        raise ValueError("x must be a contiguous 2-D tensor")
+    c, steps = _coeff_array(coeffs)
+    r, nr = _int_array(restarts)
+    _check(lib().dmuon_ns(_ptr(x), x.shape[0], x.shape[1], c, steps, r, nr, _backend(backend), float(eps),
+                          _stream(stream)))
+    return x
+
+
+def _grad_dtype(grads):
+    import torch
+    dts = {g.dtype for g in grads}
+    if dts == {torch.float32}:
+        return F32
+    if dts == {torch.bfloat16}:
+        return BF16
+    raise ValueError("grads must all be float32 or all bfloat16")
+
+
+def muon_step(params: Sequence, grads: Sequence, momenta: Sequence, lr=0.02, beta=0.95, coeffs=POLAR_EXPRESS,
+              restarts=DEFAULT_RESTARTS, backend="gram", eps=1e-7, norms_out=None, stream=None):
+    """One batched owner-rank Muon update: M <- beta M + G; W <- W - lr NS(M / (||M|| + eps))."""
+    n = len(params)
+    if not (len(grads) == len(momenta) == n) or n == 0:
+        raise ValueError("params, grads and momenta must be non-empty lists of equal length")
+    for w, g, m in zip(params, grads, momenta):
+        if w.shape != g.shape or w.shape != m.shape or w.dim() != 2:
+            raise ValueError("each param, grad and momentum must be a 2-D tensor of the same shape")
+        if not (w.is_contiguous() and g.is_contiguous() and m.is_contiguous()):
+            raise ValueError("tensors must be contiguous")
+    c, steps = _coeff_array(coeffs)
+    r, nr = _int_array(restarts)
+    P = (ctypes.c_void_p * n)(*[_ptr(t) for t in params])
+    G = (ctypes.c_void_p * n)(*[_ptr(t) for t in grads])
+    M = (ctypes.c_void_p * n)(*[_ptr(t) for t in momenta])
+    rows = (ctypes.c_int64 * n)(*[t.shape[0] for t in params])
+    cols = (ctypes.c_int64 * n)(*[t.shape[1] for t in params])
+    _check(lib().dmuon_muon_step(n, P, G, _grad_dtype(grads), M, rows, cols, _ptr(norms_out), float(lr),
+                                 float(beta), c, steps, r, nr, _backend(backend), float(eps), _stream(stream)))
+
+
+def momentum_normalize(grads, momenta, x_out, norms_out, beta=0.95, eps=1e-7, stream=None):
+    """M <- beta M + G (grads may be None), norms_out[i] = ||M_i||, x_out[i] = fp16(M_i / (||M_i|| + eps)),
+    oriented so rows <= cols."""
+    n = len(momenta)
+    gd = F32 if grads is None else _grad_dtype(grads)
+    G = None if grads is None else (ctypes.c_void_p * n)(*[_ptr(t) for t in grads])
+    M = (ctypes.c_void_p * n)(*[_ptr(t) for t in momenta])
+    X = (ctypes.c_void_p * n)(*[_ptr(t) for t in x_out])
+    rows = (ctypes.c_int64 * n)(*[t.shape[0] for t in momenta])
+    cols = (ctypes.c_int64 * n)(*[t.shape[1] for t in momenta])
+    _check(lib().dmuon_momentum_normalize(n, G, gd, M, rows, cols, X, _ptr(norms_out), float(beta), float(eps),
+                                          _stream(stream)))
+
+
+def gemm_f16(a, b, d, b_trans=True, e=None, alpha=1.0, beta=0.0, gamma=0.0, symmetric=False, stream=None):
+    """D = fp16(alpha * A Bop + beta * E + gamma * I), Bop = B^T (b_trans) or B. fp16 CUDA tensors,
+    rows contiguous (leading dimension = stride(0))."""
+    M, K = a.shape
+    N = b.shape[0] if b_trans else b.shape[1]
+    _check(lib().dmuon_gemm_f16(M, N, K, _ptr(a), a.stride(0), _ptr(b), b.stride(0), 1 if b_trans else 0, _ptr(e),
+                                e.stride(0) if e is not None else 0, _ptr(d), d.stride(0), float(alpha), float(beta),
+                                float(gamma), 1 if symmetric else 0, _stream(stream)))
+    return d
+
+
+def check_status(stream=None):
+    """Synchronise the stream and raise DmuonError if a kernel reported a timeout or a non-finite value."""
+    _check(lib().dmuon_check_status(_stream(stream)))
+
+
+def set_workspace_limit(nbytes):
+    _check(lib().dmuon_set_workspace_limit(int(nbytes)))
+
+
+def workspace_size(shapes, backend="gram"):
+    n = len(shapes)
+    rows = (ctypes.c_int64 * n)(*[s[0] for s in shapes])
+    cols = (ctypes.c_int64 * n)(*[s[1] for s in shapes])
+    out = ctypes.c_size_t(0)
+    _check(lib().dmuon_workspace_size(n, rows, cols, _backend(backend), ctypes.byref(out)))
+    return out.value
+
+
+def release_workspace():
+    _check(lib().dmuon_release_workspace())
+
+
+def gram_flops(m, n, steps=5, restarts=DEFAULT_RESTARTS):
+    """Algorithmic flops of Gram NS on one matrix (m <= n after orientation), symmetric products at half:
+    X X^T m^2 n; per step R^2 m^3, Q update 2 m^3 unless right after a (re)start, R update 3 m^3 when the
+    next step exists and is not a restart; restart Q X 2 m^2 n + X X^T m^2 n; output Q X 2 m^2 n."""
+    m, n = min(m, n), max(m, n)
+    rs = {k for k in restarts if 0 < k < steps}
+    f, fresh = m * m * n, True
+    for k in range(steps):
+        if k in rs:
+            f += 3 * m * m * n
+            fresh = True
+        f += m ** 3 + (0 if fresh else 2 * m ** 3)
+        fresh = False
+        if k + 1 < steps and (k + 1) not in rs:
+            f += 3 * m ** 3
+    return f + 2 * m * m * n
+
+
+def direct_flops(m, n, steps=5):
+    """Algorithmic flops of direct NS on one matrix, symmetric products at half: per step
+    X X^T m^2 n, A^2 m^3, B X 2 m^2 n."""
+    m, n = min(m, n), max(m, n)
+    return steps * (3 * m * m * n + m ** 3)

@@ -1,0 +1,803 @@
+// Host layer of libdmuon: argument validation, status codes, the per-device workspace, the plan
+// (workspace layout + grouped job/tile lists of every phase) and the C entry points of dmuon.h.
+//
+// Phase order of the Gram form ("Newton-Schulz 变体", sections "Gram 空间 NS（Dao-AILab）" and
+// "重启机制"), per step k with coefficients (a, b, c), on every matrix at once:
+//   start:            R = X X^T                                   (symmetric, K = n)
+//   restart before k: X' = Q X ; R = X' X'^T ; Q = I              (K = m, then K = n)
+//   step k:           Z = b R + c R^2  [Q = Z + a I after a (re)start]   (symmetric, K = m)
+//                     Q' = Z Q + a Q   (otherwise)                        (K = m)
+//                     S = Z R + a R ; R = S Z + a S   when step k+1 exists and is not a restart,
+//                                                     i.e. R <- (aI+Z) R (aI+Z)
+//   output:           W <- W - lr * (Q X), written in the caller's orientation.
+// Direct form ("直接空间 NS（经典）"), per step: A = X X^T ; B = b A + c A^2 ; X' = B X + a X, the
+// last step writing W <- W - lr * X' instead of X'.
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "dmuon.h"
+#include "internal.h"
+
+namespace dmuon {
+namespace {
+
+__device__ unsigned g_status_word;  // device status word (kDevTimeout | kDevNonfinite)
+
+thread_local std::string t_last_error;
+
+int fail(int status, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  t_last_error = buf;
+  return status;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(DMUON_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+#define DM_CUDA(call, what)                   \
+  do {                                        \
+    cudaError_t e_ = (call);                  \
+    if (e_ != cudaSuccess) return cuda_fail(e_, what); \
+  } while (0)
+
+constexpr size_t kNone = ~size_t(0);
+constexpr int64_t kMaxDim = int64_t(1) << 24;
+
+int64_t round_up(int64_t v, int64_t a) { return (v + a - 1) / a * a; }
+
+enum PlanKind { kPlanNs = 0, kPlanMuon = 1, kPlanMomNorm = 2 };
+
+struct PlanKey {
+  int kind = -1, backend = 0, steps = 0, gdtype = 0;
+  std::vector<int> restarts;
+  std::vector<int64_t> rows, cols;
+  std::vector<uintptr_t> ptrs;  // W, G, M, X_out per matrix
+  bool operator==(const PlanKey& o) const {
+    return kind == o.kind && backend == o.backend && steps == o.steps && gdtype == o.gdtype &&
+           restarts == o.restarts && rows == o.rows && cols == o.cols && ptrs == o.ptrs;
+  }
+};
+
+struct MatInfo {
+  int64_t rows, cols, m, n, ldx, ldm;
+  bool trans;
+  const void* G;
+  float* M;
+  float* W;
+  void* xout;  // caller's fp16 X (momentum_normalize only)
+  size_t X = kNone, Xb = kNone, R = kNone, Z = kNone, Q = kNone, Qb = kNone, S = kNone;
+};
+
+// One product in a phase; operands are arena offsets (kNone = unused), resolved when bound.
+struct JobSpec {
+  int mat;
+  int M, N, K;
+  int recipe, flags;
+  size_t a, b, e, d, d2;
+  int64_t lda, ldb, lde, ldd;
+  float* W;
+  int64_t ldw;
+};
+
+struct LaunchRec {
+  int first_job, njobs, first_tile, ntiles, bn, coef;
+};
+
+struct Plan {
+  PlanKey key;
+  bool bound = false;
+  std::vector<MatInfo> mats;
+  std::vector<std::vector<JobSpec>> phases;  // one grouped launch each
+  std::vector<int> phase_coef;
+  int64_t nchunks = 0, ncast = 0;
+  size_t off_rowmats = 0, off_chunk = 0, off_tilep = 0, off_partials = 0, off_norms = 0, off_inv = 0;
+  size_t off_jobs = 0, off_tiles = 0, bytes = 0;
+  // host images uploaded to the arena
+  std::vector<RowMat> rowmats;
+  std::vector<int64_t> chunk_prefix, tile_prefix;
+  std::vector<GemmJob> jobs;
+  std::vector<GemmTile> tiles;
+  std::vector<LaunchRec> launches;
+};
+
+struct Layout {
+  size_t off = 0;
+  size_t take(size_t bytes, size_t align = 256) {
+    off = (off + align - 1) / align * align;
+    const size_t r = off;
+    off += bytes;
+    return r;
+  }
+};
+
+struct DeviceState {
+  bool init = false;
+  int sms = 0;
+  unsigned* status = nullptr;
+  char* arena = nullptr;
+  size_t arena_bytes = 0;
+  Plan plan;
+};
+
+std::mutex g_mu;
+constexpr int kMaxDevices = 64;
+DeviceState g_dev[kMaxDevices];
+size_t g_ws_limit = 0;
+
+int current_device(DeviceState** out) {
+  int dev = 0;
+  DM_CUDA(cudaGetDevice(&dev), "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(DMUON_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+  DeviceState& ds = g_dev[dev];
+  if (!ds.init) {
+    int major = 0, minor = 0;
+    DM_CUDA(cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev), "cudaDeviceGetAttribute");
+    DM_CUDA(cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev), "cudaDeviceGetAttribute");
+    if (major != 10 || minor != 3)
+      return fail(DMUON_ERR_UNSUPPORTED, "libdmuon is built for sm_103a (GB300); device %d is sm_%d%d", dev,
+                  major, minor);
+    DM_CUDA(cudaDeviceGetAttribute(&ds.sms, cudaDevAttrMultiProcessorCount, dev), "cudaDeviceGetAttribute");
+    void* addr = nullptr;
+    DM_CUDA(cudaGetSymbolAddress(&addr, g_status_word), "cudaGetSymbolAddress(status word)");
+    ds.status = static_cast<unsigned*>(addr);
+    DM_CUDA(cudaMemset(ds.status, 0, sizeof(unsigned)), "cudaMemset(status word)");
+    ds.init = true;
+  }
+  *out = &ds;
+  return DMUON_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+int check_ns_args(const float* coeffs, int steps, const int* restarts, int n_restarts, int backend, float eps) {
+  if (backend != DMUON_NS_DIRECT && backend != DMUON_NS_GRAM)
+    return fail(DMUON_ERR_INVALID_ARG, "backend must be DMUON_NS_DIRECT (0) or DMUON_NS_GRAM (1), got %d", backend);
+  if (steps < 1 || steps > DMUON_MAX_STEPS)
+    return fail(DMUON_ERR_INVALID_ARG, "steps must be in [1, %d], got %d", DMUON_MAX_STEPS, steps);
+  if (!coeffs) return fail(DMUON_ERR_INVALID_ARG, "coeffs is NULL");
+  for (int i = 0; i < 3 * steps; ++i)
+    if (!std::isfinite(coeffs[i])) return fail(DMUON_ERR_INVALID_ARG, "coeffs[%d] is not finite", i);
+  if (n_restarts < 0) return fail(DMUON_ERR_INVALID_ARG, "n_restarts must be >= 0");
+  if (n_restarts > 0 && !restarts) return fail(DMUON_ERR_INVALID_ARG, "restarts is NULL with n_restarts > 0");
+  for (int i = 0; i < n_restarts; ++i) {
+    if (restarts[i] < 0 || restarts[i] >= steps)
+      return fail(DMUON_ERR_INVALID_ARG, "restart index %d outside [0, steps-1]", restarts[i]);
+    if (i > 0 && restarts[i] <= restarts[i - 1])
+      return fail(DMUON_ERR_INVALID_ARG, "restart indices must be strictly increasing");
+  }
+  if (!(eps >= 0.f) || !std::isfinite(eps)) return fail(DMUON_ERR_INVALID_ARG, "eps must be finite and >= 0");
+  return DMUON_OK;
+}
+
+// ---------------------------------------------------------------------------- plan building
+
+JobSpec make_job(int mat, int M, int N, int K, int recipe, int flags, size_t a, int64_t lda, size_t b, int64_t ldb,
+                 size_t e, int64_t lde, size_t d, int64_t ldd, size_t d2 = kNone) {
+  JobSpec j;
+  j.mat = mat;
+  j.M = M, j.N = N, j.K = K;
+  j.recipe = recipe, j.flags = flags;
+  j.a = a, j.b = b, j.e = e, j.d = d, j.d2 = d2;
+  j.lda = lda, j.ldb = ldb, j.lde = lde, j.ldd = ldd;
+  j.W = nullptr;
+  j.ldw = 0;
+  return j;
+}
+
+void build_gram_phases(Plan& pl, const std::vector<int>& restarts, int steps) {
+  const int nm = static_cast<int>(pl.mats.size());
+  std::vector<char> is_restart(steps + 1, 0);
+  for (int r : restarts)
+    if (r > 0 && r < steps) is_restart[r] = 1;
+  std::vector<size_t> X(nm), Xb(nm), Q(nm), Qb(nm);
+  for (int i = 0; i < nm; ++i) X[i] = pl.mats[i].X, Xb[i] = pl.mats[i].Xb, Q[i] = pl.mats[i].Q, Qb[i] = pl.mats[i].Qb;
+
+  auto push = [&](std::vector<JobSpec>&& ph, int coef) {
+    if (!ph.empty()) {
+      pl.phases.push_back(std::move(ph));
+      pl.phase_coef.push_back(coef);
+    }
+  };
+  auto gram_of_x = [&](int coef) {
+    std::vector<JobSpec> ph;
+    for (int i = 0; i < nm; ++i) {
+      const MatInfo& mi = pl.mats[i];
+      ph.push_back(make_job(i, mi.m, mi.m, mi.n, kRecPlain, kJobSymmetric, X[i], mi.ldx, X[i], mi.ldx, kNone, 0,
+                            mi.R, mi.ldm));
+    }
+    push(std::move(ph), coef);
+  };
+
+  gram_of_x(0);
+  bool fresh = true;
+  for (int k = 0; k < steps; ++k) {
+    if (is_restart[k]) {
+      std::vector<JobSpec> ph;
+      for (int i = 0; i < nm; ++i) {
+        const MatInfo& mi = pl.mats[i];
+        ph.push_back(make_job(i, mi.m, mi.n, mi.m, kRecPlain, kJobBMnMajor, Q[i], mi.ldm, X[i], mi.ldx, kNone, 0,
+                              Xb[i], mi.ldx));
+        std::swap(X[i], Xb[i]);
+      }
+      push(std::move(ph), k);
+      gram_of_x(k);
+      fresh = true;
+    }
+    {  // Z = b R + c R^2 (and the first Q after a (re)start)
+      std::vector<JobSpec> ph;
+      for (int i = 0; i < nm; ++i) {
+        const MatInfo& mi = pl.mats[i];
+        ph.push_back(make_job(i, mi.m, mi.m, mi.m, kRecZ, kJobSymmetric | (fresh ? kJobD2 : 0), mi.R, mi.ldm, mi.R,
+                              mi.ldm, mi.R, mi.ldm, mi.Z, mi.ldm, fresh ? Q[i] : kNone));
+      }
+      push(std::move(ph), k);
+    }
+    const bool update_r = (k + 1 < steps) && !is_restart[k + 1];
+    {
+      std::vector<JobSpec> ph;
+      for (int i = 0; i < nm; ++i) {
+        const MatInfo& mi = pl.mats[i];
+        if (!fresh) {  // Q' = Z Q + a Q
+          ph.push_back(make_job(i, mi.m, mi.m, mi.m, kRecAxpy, kJobBMnMajor, mi.Z, mi.ldm, Q[i], mi.ldm, Q[i], mi.ldm,
+                                Qb[i], mi.ldm));
+        }
+        if (update_r) {  // S = Z R + a R
+          ph.push_back(make_job(i, mi.m, mi.m, mi.m, kRecAxpy, 0, mi.Z, mi.ldm, mi.R, mi.ldm, mi.R, mi.ldm, mi.S,
+                                mi.ldm));
+        }
+      }
+      push(std::move(ph), k);
+      if (!fresh)
+        for (int i = 0; i < nm; ++i) std::swap(Q[i], Qb[i]);
+    }
+    if (update_r) {  // R = S Z + a S (symmetric)
+      std::vector<JobSpec> ph;
+      for (int i = 0; i < nm; ++i) {
+        const MatInfo& mi = pl.mats[i];
+        ph.push_back(make_job(i, mi.m, mi.m, mi.m, kRecAxpy, kJobSymmetric, mi.S, mi.ldm, mi.Z, mi.ldm, mi.S, mi.ldm,
+                              mi.R, mi.ldm));
+      }
+      push(std::move(ph), k);
+    }
+    fresh = false;
+  }
+  {  // output: W <- w_alpha W + w_beta (Q X)
+    std::vector<JobSpec> ph;
+    for (int i = 0; i < nm; ++i) {
+      const MatInfo& mi = pl.mats[i];
+      JobSpec j = make_job(i, mi.m, mi.n, mi.m, kRecPlain, kJobBMnMajor | kJobFinal | (mi.trans ? kJobFinalTrans : 0),
+                           Q[i], mi.ldm, X[i], mi.ldx, kNone, 0, kNone, 0);
+      j.W = mi.W;
+      j.ldw = mi.cols;
+      ph.push_back(j);
+    }
+    push(std::move(ph), steps - 1);
+  }
+}
+
+void build_direct_phases(Plan& pl, int steps) {
+  const int nm = static_cast<int>(pl.mats.size());
+  std::vector<size_t> X(nm), Xb(nm);
+  for (int i = 0; i < nm; ++i) X[i] = pl.mats[i].X, Xb[i] = pl.mats[i].Xb;
+  for (int k = 0; k < steps; ++k) {
+    std::vector<JobSpec> p1, p2, p3;
+    for (int i = 0; i < nm; ++i) {
+      const MatInfo& mi = pl.mats[i];
+      // A = X X^T (in R), B = b A + c A^2 (in Z)
+      p1.push_back(make_job(i, mi.m, mi.m, mi.n, kRecPlain, kJobSymmetric, X[i], mi.ldx, X[i], mi.ldx, kNone, 0, mi.R,
+                            mi.ldm));
+      p2.push_back(make_job(i, mi.m, mi.m, mi.m, kRecZ, kJobSymmetric, mi.R, mi.ldm, mi.R, mi.ldm, mi.R, mi.ldm, mi.Z,
+                            mi.ldm));
+      if (k + 1 < steps) {  // X' = B X + a X
+        p3.push_back(make_job(i, mi.m, mi.n, mi.m, kRecAxpy, kJobBMnMajor, mi.Z, mi.ldm, X[i], mi.ldx, X[i], mi.ldx,
+                              Xb[i], mi.ldx));
+      } else {
+        JobSpec j = make_job(i, mi.m, mi.n, mi.m, kRecAxpy, kJobBMnMajor | kJobFinal | (mi.trans ? kJobFinalTrans : 0),
+                             mi.Z, mi.ldm, X[i], mi.ldx, X[i], mi.ldx, kNone, 0);
+        j.W = mi.W;
+        j.ldw = mi.cols;
+        p3.push_back(j);
+      }
+    }
+    pl.phases.push_back(std::move(p1));
+    pl.phase_coef.push_back(k);
+    pl.phases.push_back(std::move(p2));
+    pl.phase_coef.push_back(k);
+    pl.phases.push_back(std::move(p3));
+    pl.phase_coef.push_back(k);
+    if (k + 1 < steps)
+      for (int i = 0; i < nm; ++i) std::swap(X[i], Xb[i]);
+  }
+}
+
+int launch_bn(const std::vector<JobSpec>& ph) {
+  for (const JobSpec& j : ph)
+    if (j.N > 128) return 256;
+  return 128;
+}
+
+// Host-side plan: matrix layout, workspace offsets, phases, tiles. No device calls.
+int build_plan_host(Plan& pl, const PlanKey& key, const std::vector<const void*>& G, const std::vector<float*>& Mom,
+                    const std::vector<float*>& W, const std::vector<void*>& xout) {
+  pl = Plan();
+  pl.key = key;
+  const int nm = static_cast<int>(key.rows.size());
+  Layout lay;
+  pl.off_rowmats = lay.take(sizeof(RowMat) * nm);
+  pl.off_chunk = lay.take(sizeof(int64_t) * (nm + 1));
+  pl.off_tilep = lay.take(sizeof(int64_t) * (nm + 1));
+  pl.chunk_prefix.assign(nm + 1, 0);
+  pl.tile_prefix.assign(nm + 1, 0);
+  pl.mats.resize(nm);
+  for (int i = 0; i < nm; ++i) {
+    MatInfo& mi = pl.mats[i];
+    mi.rows = key.rows[i];
+    mi.cols = key.cols[i];
+    mi.trans = mi.rows > mi.cols;
+    mi.m = std::min(mi.rows, mi.cols);
+    mi.n = std::max(mi.rows, mi.cols);
+    mi.ldx = key.kind == kPlanMomNorm ? mi.n : round_up(mi.n, 8);
+    mi.ldm = round_up(mi.m, 8);
+    mi.G = G[i];
+    mi.M = Mom[i];
+    mi.W = W[i];
+    mi.xout = xout[i];
+    const int64_t numel = mi.rows * mi.cols;
+    pl.chunk_prefix[i + 1] = pl.chunk_prefix[i] + (numel + kChunkElems - 1) / kChunkElems;
+    pl.tile_prefix[i + 1] =
+        pl.tile_prefix[i] + ((mi.rows + kCastTile - 1) / kCastTile) * ((mi.cols + kCastTile - 1) / kCastTile);
+  }
+  pl.nchunks = pl.chunk_prefix[nm];
+  pl.ncast = pl.tile_prefix[nm];
+  if (pl.nchunks >= (int64_t(1) << 31) || pl.ncast >= (int64_t(1) << 31))
+    return fail(DMUON_ERR_UNSUPPORTED, "too many elements in one call");
+  pl.off_partials = lay.take(sizeof(float) * pl.nchunks);
+  pl.off_norms = lay.take(sizeof(float) * nm);
+  pl.off_inv = lay.take(sizeof(float) * nm);
+  const bool gram = key.backend == DMUON_NS_GRAM;
+  for (int i = 0; i < nm; ++i) {
+    MatInfo& mi = pl.mats[i];
+    if (key.kind == kPlanMomNorm) continue;
+    const size_t xbytes = sizeof(__half) * mi.m * mi.ldx;
+    const size_t mbytes = sizeof(__half) * mi.m * mi.ldm;
+    mi.X = lay.take(xbytes);
+    mi.Xb = lay.take(xbytes);
+    mi.R = lay.take(mbytes);
+    mi.Z = lay.take(mbytes);
+    if (gram) {
+      mi.Q = lay.take(mbytes);
+      mi.Qb = lay.take(mbytes);
+      mi.S = lay.take(mbytes);
+    }
+  }
+  pl.rowmats.resize(nm);
+  int part = 0;
+  for (int i = 0; i < nm; ++i) {
+    const MatInfo& mi = pl.mats[i];
+    RowMat& r = pl.rowmats[i];
+    std::memset(&r, 0, sizeof(r));
+    r.G = mi.G;
+    r.M = mi.M;
+    r.rows = mi.rows;
+    r.cols = mi.cols;
+    r.ldx = mi.ldx;
+    r.gdtype = key.gdtype;
+    r.trans = mi.trans ? 1 : 0;
+    r.vec_ok = 1;  // pointers are validated 16-byte aligned
+    r.part_begin = part;
+    r.part_count = static_cast<int>(pl.chunk_prefix[i + 1] - pl.chunk_prefix[i]);
+    part += r.part_count;
+  }
+  if (key.kind != kPlanMomNorm) {
+    if (gram) build_gram_phases(pl, key.restarts, key.steps);
+    else build_direct_phases(pl, key.steps);
+  }
+  // Tiles: per launch, jobs in decreasing K (longest first), tiles row-major within a job.
+  size_t njobs = 0;
+  for (auto& ph : pl.phases) {
+    std::stable_sort(ph.begin(), ph.end(), [](const JobSpec& x, const JobSpec& y) { return x.K > y.K; });
+    njobs += ph.size();
+  }
+  for (size_t p = 0; p < pl.phases.size(); ++p) {
+    const auto& ph = pl.phases[p];
+    LaunchRec L;
+    L.first_job = 0;  // filled below
+    L.njobs = static_cast<int>(ph.size());
+    L.bn = launch_bn(ph);
+    L.coef = pl.phase_coef[p];
+    L.first_tile = static_cast<int>(pl.tiles.size());
+    for (int j = 0; j < L.njobs; ++j) {
+      const JobSpec& js = ph[j];
+      const int tm_n = (js.M + kBM - 1) / kBM;
+      const int tn_n = (js.N + L.bn - 1) / L.bn;
+      for (int tm = 0; tm < tm_n; ++tm)
+        for (int tn = 0; tn < tn_n; ++tn) {
+          if ((js.flags & kJobSymmetric) && tn * L.bn + L.bn - 1 < tm * kBM) continue;
+          pl.tiles.push_back(GemmTile{j, tm, tn, 0});
+        }
+    }
+    L.ntiles = static_cast<int>(pl.tiles.size()) - L.first_tile;
+    pl.launches.push_back(L);
+  }
+  int acc = 0;
+  for (auto& L : pl.launches) L.first_job = acc, acc += L.njobs;
+  if (pl.tiles.size() >= (size_t(1) << 31)) return fail(DMUON_ERR_UNSUPPORTED, "too many tiles in one call");
+  pl.off_jobs = lay.take(sizeof(GemmJob) * std::max<size_t>(njobs, 1), 256);
+  pl.off_tiles = lay.take(sizeof(GemmTile) * std::max<size_t>(pl.tiles.size(), 1));
+  pl.bytes = lay.off;
+  return DMUON_OK;
+}
+
+// Place the plan in the device arena, resolve operand addresses, encode tensor maps and upload.
+int bind_plan(DeviceState& ds, Plan& pl, cudaStream_t stream) {
+  if (g_ws_limit && pl.bytes > g_ws_limit)
+    return fail(DMUON_ERR_OOM, "workspace of %zu bytes exceeds the limit of %zu bytes", pl.bytes, g_ws_limit);
+  DM_CUDA(cudaDeviceSynchronize(), "cudaDeviceSynchronize before re-planning");
+  if (pl.bytes > ds.arena_bytes) {
+    if (ds.arena) {
+      cudaFree(ds.arena);
+      ds.arena = nullptr;
+      ds.arena_bytes = 0;
+    }
+    const size_t want = pl.bytes + (pl.bytes >> 4);
+    if (cudaMalloc(&ds.arena, want) != cudaSuccess) {
+      cudaGetLastError();
+      ds.arena = nullptr;
+      return fail(DMUON_ERR_OOM, "cudaMalloc of %zu workspace bytes failed", want);
+    }
+    ds.arena_bytes = want;
+  }
+  char* base = ds.arena;
+  auto at = [&](size_t off) -> void* { return off == kNone ? nullptr : base + off; };
+  for (size_t i = 0; i < pl.mats.size(); ++i) {
+    pl.rowmats[i].X = static_cast<__half*>(pl.key.kind == kPlanMomNorm ? pl.mats[i].xout : at(pl.mats[i].X));
+  }
+  pl.jobs.clear();
+  for (size_t p = 0; p < pl.phases.size(); ++p) {
+    const int bn = pl.launches[p].bn;
+    for (const JobSpec& js : pl.phases[p]) {
+      GemmJob j;
+      std::memset(&j, 0, sizeof(j));
+      j.M = js.M, j.N = js.N, j.K = js.K;
+      j.recipe = js.recipe, j.flags = js.flags;
+      j.D = static_cast<__half*>(at(js.d));
+      j.D2 = static_cast<__half*>(at(js.d2));
+      j.E = static_cast<const __half*>(at(js.e));
+      j.W = js.W;
+      j.ldd = js.ldd, j.lde = js.lde, j.ldw = js.ldw;
+      j.tiles_n = (js.N + bn - 1) / bn;
+      const char* err = nullptr;
+      if (!encode_job_maps(j, at(js.a), js.lda, at(js.b), js.ldb, (js.flags & kJobBMnMajor) != 0, bn, &err))
+        return fail(DMUON_ERR_CUDA, "%s", err);
+      pl.jobs.push_back(j);
+    }
+  }
+  DM_CUDA(cudaMemcpyAsync(base + pl.off_rowmats, pl.rowmats.data(), sizeof(RowMat) * pl.rowmats.size(),
+                          cudaMemcpyHostToDevice, stream), "upload matrix table");
+  DM_CUDA(cudaMemcpyAsync(base + pl.off_chunk, pl.chunk_prefix.data(), sizeof(int64_t) * pl.chunk_prefix.size(),
+                          cudaMemcpyHostToDevice, stream), "upload chunk table");
+  DM_CUDA(cudaMemcpyAsync(base + pl.off_tilep, pl.tile_prefix.data(), sizeof(int64_t) * pl.tile_prefix.size(),
+                          cudaMemcpyHostToDevice, stream), "upload tile table");
+  if (!pl.jobs.empty())
+    DM_CUDA(cudaMemcpyAsync(base + pl.off_jobs, pl.jobs.data(), sizeof(GemmJob) * pl.jobs.size(),
+                            cudaMemcpyHostToDevice, stream), "upload job table");
+  if (!pl.tiles.empty())
+    DM_CUDA(cudaMemcpyAsync(base + pl.off_tiles, pl.tiles.data(), sizeof(GemmTile) * pl.tiles.size(),
+                            cudaMemcpyHostToDevice, stream), "upload tile list");
+  pl.bound = true;
+  return DMUON_OK;
+}
+
+int run_plan(DeviceState& ds, const Plan& pl, const float* coeffs, float lr, float beta, float eps, float* norms_out,
+             cudaStream_t stream) {
+  char* base = ds.arena;
+  RowLaunch rl;
+  rl.mats = reinterpret_cast<const RowMat*>(base + pl.off_rowmats);
+  rl.nmats = static_cast<int>(pl.mats.size());
+  rl.chunk_prefix = reinterpret_cast<const int64_t*>(base + pl.off_chunk);
+  rl.tile_prefix = reinterpret_cast<const int64_t*>(base + pl.off_tilep);
+  rl.partials = reinterpret_cast<float*>(base + pl.off_partials);
+  rl.norms = reinterpret_cast<float*>(base + pl.off_norms);
+  rl.inv = reinterpret_cast<float*>(base + pl.off_inv);
+  rl.norms_out = norms_out;
+  rl.beta = beta;
+  rl.eps = eps;
+  DM_CUDA(launch_momentum_sumsq(rl, pl.nchunks, stream), "momentum/sum-of-squares launch");
+  DM_CUDA(launch_finalize_norms(rl, stream), "norm launch");
+  DM_CUDA(launch_normalize_cast(rl, pl.ncast, stream), "normalise/cast launch");
+  const GemmJob* jobs = reinterpret_cast<const GemmJob*>(base + pl.off_jobs);
+  const GemmTile* tiles = reinterpret_cast<const GemmTile*>(base + pl.off_tiles);
+  for (const LaunchRec& L : pl.launches) {
+    GemmLaunch gl;
+    std::memset(&gl, 0, sizeof(gl));
+    gl.jobs = jobs + L.first_job;
+    gl.tiles = tiles + L.first_tile;
+    gl.ntiles = L.ntiles;
+    gl.a = coeffs[3 * L.coef + 0];
+    gl.b = coeffs[3 * L.coef + 1];
+    gl.c = coeffs[3 * L.coef + 2];
+    gl.w_alpha = pl.key.kind == kPlanNs ? 0.f : 1.f;
+    gl.w_beta = pl.key.kind == kPlanNs ? 1.f : -lr;
+    gl.status = ds.status;
+    const int grid = std::min(L.ntiles, ds.sms);
+    DM_CUDA(launch_gemm(gl, L.bn, grid, stream), "tensor-core GEMM launch");
+  }
+  return DMUON_OK;
+}
+
+// Shared body of the three plan-based entry points.
+int plan_and_run(const PlanKey& key, const std::vector<const void*>& G, const std::vector<float*>& Mom,
+                 const std::vector<float*>& W, const std::vector<void*>& xout, const float* coeffs, float lr,
+                 float beta, float eps, float* norms_out, cudaStream_t stream) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState* ds = nullptr;
+  int st = current_device(&ds);
+  if (st != DMUON_OK) return st;
+  if (!(ds->plan.bound && ds->plan.key == key)) {
+    ds->plan = Plan();
+    st = build_plan_host(ds->plan, key, G, Mom, W, xout);
+    if (st != DMUON_OK) return st;
+    st = bind_plan(*ds, ds->plan, stream);
+    if (st != DMUON_OK) {
+      ds->plan = Plan();
+      return st;
+    }
+  }
+  return run_plan(*ds, ds->plan, coeffs, lr, beta, eps, norms_out, stream);
+}
+
+int check_matrix_list(int count, const int64_t* rows, const int64_t* cols) {
+  if (count < 1) return fail(DMUON_ERR_INVALID_ARG, "count must be >= 1");
+  if (!rows || !cols) return fail(DMUON_ERR_INVALID_ARG, "rows/cols arrays are NULL");
+  for (int i = 0; i < count; ++i) {
+    if (rows[i] < 1 || cols[i] < 1)
+      return fail(DMUON_ERR_INVALID_ARG, "matrix %d has a non-positive size (%lld x %lld)", i, (long long)rows[i],
+                  (long long)cols[i]);
+    if (rows[i] > kMaxDim || cols[i] > kMaxDim)
+      return fail(DMUON_ERR_UNSUPPORTED, "matrix %d is larger than %lld in one dimension", i, (long long)kMaxDim);
+  }
+  return DMUON_OK;
+}
+
+}  // namespace
+}  // namespace dmuon
+
+using namespace dmuon;
+
+extern "C" {
+
+int dmuon_ns(float* x, int64_t m, int64_t n, const float* coeffs, int steps, const int* restarts, int n_restarts,
+             int backend, float eps, void* cuda_stream) {
+  try {
+    if (!x) return fail(DMUON_ERR_INVALID_ARG, "x is NULL");
+    if (!aligned16(x)) return fail(DMUON_ERR_INVALID_ARG, "x must be 16-byte aligned");
+    int st = check_matrix_list(1, &m, &n);
+    if (st != DMUON_OK) return st;
+    st = check_ns_args(coeffs, steps, restarts, n_restarts, backend, eps);
+    if (st != DMUON_OK) return st;
+    PlanKey key;
+    key.kind = kPlanNs;
+    key.backend = backend;
+    key.steps = steps;
+    key.gdtype = 0;
+    if (backend == DMUON_NS_GRAM) key.restarts.assign(restarts, restarts + n_restarts);
+    key.rows = {m};
+    key.cols = {n};
+    key.ptrs = {reinterpret_cast<uintptr_t>(x)};
+    return plan_and_run(key, {nullptr}, {x}, {x}, {nullptr}, coeffs, 0.f, 0.f, eps, nullptr,
+                        static_cast<cudaStream_t>(cuda_stream));
+  } catch (const std::exception& e) {
+    return fail(DMUON_ERR_OOM, "host exception: %s", e.what());
+  }
+}
+
+int dmuon_muon_step(int count, float* const* params, const void* const* grads, int grad_dtype, float* const* momenta,
+                    const int64_t* rows, const int64_t* cols, float* norms_out, float lr, float beta,
+                    const float* coeffs, int steps, const int* restarts, int n_restarts, int backend, float eps,
+                    void* cuda_stream) {
+  try {
+    int st = check_matrix_list(count, rows, cols);
+    if (st != DMUON_OK) return st;
+    if (!params || !grads || !momenta) return fail(DMUON_ERR_INVALID_ARG, "params/grads/momenta arrays are NULL");
+    if (grad_dtype != DMUON_F32 && grad_dtype != DMUON_BF16)
+      return fail(DMUON_ERR_INVALID_ARG, "grad_dtype must be DMUON_F32 (0) or DMUON_BF16 (1)");
+    if (!std::isfinite(lr) || !std::isfinite(beta)) return fail(DMUON_ERR_INVALID_ARG, "lr and beta must be finite");
+    if (norms_out && !aligned16(norms_out) && (reinterpret_cast<uintptr_t>(norms_out) & 3))
+      return fail(DMUON_ERR_INVALID_ARG, "norms_out must be 4-byte aligned");
+    st = check_ns_args(coeffs, steps, restarts, n_restarts, backend, eps);
+    if (st != DMUON_OK) return st;
+    PlanKey key;
+    key.kind = kPlanMuon;
+    key.backend = backend;
+    key.steps = steps;
+    key.gdtype = grad_dtype;
+    if (backend == DMUON_NS_GRAM) key.restarts.assign(restarts, restarts + n_restarts);
+    key.rows.assign(rows, rows + count);
+    key.cols.assign(cols, cols + count);
+    std::vector<const void*> G(count);
+    std::vector<float*> Mo(count), W(count);
+    std::vector<void*> xo(count, nullptr);
+    for (int i = 0; i < count; ++i) {
+      if (!params[i] || !grads[i] || !momenta[i])
+        return fail(DMUON_ERR_INVALID_ARG, "matrix %d has a NULL pointer", i);
+      if (!aligned16(params[i]) || !aligned16(grads[i]) || !aligned16(momenta[i]))
+        return fail(DMUON_ERR_INVALID_ARG, "matrix %d: device buffers must be 16-byte aligned", i);
+      G[i] = grads[i];
+      Mo[i] = momenta[i];
+      W[i] = params[i];
+      key.ptrs.push_back(reinterpret_cast<uintptr_t>(params[i]));
+      key.ptrs.push_back(reinterpret_cast<uintptr_t>(grads[i]));
+      key.ptrs.push_back(reinterpret_cast<uintptr_t>(momenta[i]));
+    }
+    return plan_and_run(key, G, Mo, W, xo, coeffs, lr, beta, eps, norms_out, static_cast<cudaStream_t>(cuda_stream));
+  } catch (const std::exception& e) {
+    return fail(DMUON_ERR_OOM, "host exception: %s", e.what());
+  }
+}
+
+int dmuon_momentum_normalize(int count, const void* const* grads, int grad_dtype, float* const* momenta,
+                             const int64_t* rows, const int64_t* cols, void* const* x_out, float* norms_out,
+                             float beta, float eps, void* cuda_stream) {
+  try {
+    int st = check_matrix_list(count, rows, cols);
+    if (st != DMUON_OK) return st;
+    if (!momenta || !x_out || !norms_out) return fail(DMUON_ERR_INVALID_ARG, "momenta/x_out/norms_out are NULL");
+    if (grad_dtype != DMUON_F32 && grad_dtype != DMUON_BF16)
+      return fail(DMUON_ERR_INVALID_ARG, "grad_dtype must be DMUON_F32 (0) or DMUON_BF16 (1)");
+    if (!std::isfinite(beta) || !std::isfinite(eps) || !(eps >= 0.f))
+      return fail(DMUON_ERR_INVALID_ARG, "beta must be finite and eps finite and >= 0");
+    PlanKey key;
+    key.kind = kPlanMomNorm;
+    key.gdtype = grad_dtype;
+    key.rows.assign(rows, rows + count);
+    key.cols.assign(cols, cols + count);
+    std::vector<const void*> G(count);
+    std::vector<float*> Mo(count), W(count, nullptr);
+    std::vector<void*> xo(count);
+    for (int i = 0; i < count; ++i) {
+      const void* g = grads ? grads[i] : nullptr;
+      if (!momenta[i] || !x_out[i]) return fail(DMUON_ERR_INVALID_ARG, "matrix %d has a NULL pointer", i);
+      if (!aligned16(momenta[i]) || (g && !aligned16(g)) || !aligned16(x_out[i]))
+        return fail(DMUON_ERR_INVALID_ARG, "matrix %d: device buffers must be 16-byte aligned", i);
+      G[i] = g;
+      Mo[i] = momenta[i];
+      xo[i] = x_out[i];
+      key.ptrs.push_back(reinterpret_cast<uintptr_t>(g));
+      key.ptrs.push_back(reinterpret_cast<uintptr_t>(momenta[i]));
+      key.ptrs.push_back(reinterpret_cast<uintptr_t>(x_out[i]));
+    }
+    const float dummy[3] = {0.f, 0.f, 0.f};
+    return plan_and_run(key, G, Mo, W, xo, dummy, 0.f, beta, eps, norms_out, static_cast<cudaStream_t>(cuda_stream));
+  } catch (const std::exception& e) {
+    return fail(DMUON_ERR_OOM, "host exception: %s", e.what());
+  }
+}
+
+int dmuon_gemm_f16(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb,
+                   int b_trans, const void* E, int64_t lde, void* D, int64_t ldd, float alpha, float beta, float gamma,
+                   int symmetric, void* cuda_stream) {
+  try {
+    if (M < 1 || N < 1 || K < 1) return fail(DMUON_ERR_INVALID_ARG, "M, N, K must be >= 1");
+    if (M > kMaxDim || N > kMaxDim || K > kMaxDim) return fail(DMUON_ERR_UNSUPPORTED, "dimension above %lld", (long long)kMaxDim);
+    if (!A || !B || !D) return fail(DMUON_ERR_INVALID_ARG, "A, B and D must not be NULL");
+    if (!aligned16(A) || !aligned16(B) || !aligned16(D) || (E && !aligned16(E)))
+      return fail(DMUON_ERR_INVALID_ARG, "A, B, D, E must be 16-byte aligned");
+    if (symmetric && M != N) return fail(DMUON_ERR_INVALID_ARG, "symmetric output needs M == N");
+    const int64_t b_row = b_trans ? K : N;
+    if (lda < K || ldb < b_row || ldd < N || (E && lde < N))
+      return fail(DMUON_ERR_INVALID_ARG, "a leading dimension is smaller than its row length");
+    if ((lda | ldb | ldd | (E ? lde : 0)) & 7)
+      return fail(DMUON_ERR_INVALID_ARG, "leading dimensions must be multiples of 8 elements (16 bytes)");
+    if (!std::isfinite(alpha) || !std::isfinite(beta) || !std::isfinite(gamma))
+      return fail(DMUON_ERR_INVALID_ARG, "alpha, beta, gamma must be finite");
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceState* ds = nullptr;
+    int st = current_device(&ds);
+    if (st != DMUON_OK) return st;
+    const int bn = N > 128 ? 256 : 128;
+    GemmLaunch gl;
+    std::memset(&gl, 0, sizeof(gl));
+    GemmJob& j = gl.single;
+    j.M = static_cast<int>(M), j.N = static_cast<int>(N), j.K = static_cast<int>(K);
+    j.recipe = kRecCustom;
+    j.flags = (symmetric ? kJobSymmetric : 0) | (b_trans ? 0 : kJobBMnMajor);
+    j.D = static_cast<__half*>(D);
+    j.E = static_cast<const __half*>(E);
+    j.ldd = ldd, j.lde = E ? lde : 0;
+    j.tiles_n = static_cast<int>((N + bn - 1) / bn);
+    const char* err = nullptr;
+    if (!encode_job_maps(j, A, lda, B, ldb, !b_trans, bn, &err)) return fail(DMUON_ERR_CUDA, "%s", err);
+    gl.jobs = nullptr;
+    gl.tiles = nullptr;
+    gl.tiles_m = static_cast<int>((M + kBM - 1) / kBM);
+    const int64_t ntiles = static_cast<int64_t>(gl.tiles_m) * j.tiles_n;
+    if (ntiles >= (int64_t(1) << 31)) return fail(DMUON_ERR_UNSUPPORTED, "too many tiles");
+    gl.ntiles = static_cast<int>(ntiles);
+    gl.alpha = alpha, gl.beta = E ? beta : 0.f, gl.gamma = gamma;
+    gl.status = ds->status;
+    const int grid = static_cast<int>(std::min<int64_t>(ntiles, ds->sms));
+    DM_CUDA(launch_gemm(gl, bn, grid, static_cast<cudaStream_t>(cuda_stream)), "tensor-core GEMM launch");
+    return DMUON_OK;
+  } catch (const std::exception& e) {
+    return fail(DMUON_ERR_OOM, "host exception: %s", e.what());
+  }
+}
+
+int dmuon_check_status(void* cuda_stream) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState* ds = nullptr;
+  int st = current_device(&ds);
+  if (st != DMUON_OK) return st;
+  DM_CUDA(cudaStreamSynchronize(static_cast<cudaStream_t>(cuda_stream)), "cudaStreamSynchronize");
+  unsigned word = 0;
+  DM_CUDA(cudaMemcpy(&word, ds->status, sizeof(word), cudaMemcpyDeviceToHost), "read device status");
+  if (word) DM_CUDA(cudaMemset(ds->status, 0, sizeof(unsigned)), "clear device status");
+  if (word & kDevTimeout) return fail(DMUON_ERR_TIMEOUT, "a device-side bounded wait gave up; results are invalid");
+  if (word & kDevNonfinite) return fail(DMUON_ERR_NONFINITE, "an fp16 intermediate overflowed or was NaN");
+  return DMUON_OK;
+}
+
+const char* dmuon_last_error(void) { return t_last_error.c_str(); }
+
+const char* dmuon_version(void) { return "dmuon-gb300 0.1.0 (sm_103a)"; }
+
+int dmuon_set_workspace_limit(size_t bytes) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  g_ws_limit = bytes;
+  return DMUON_OK;
+}
+
+int dmuon_workspace_size(int count, const int64_t* rows, const int64_t* cols, int backend, size_t* bytes_out) {
+  try {
+    if (!bytes_out) return fail(DMUON_ERR_INVALID_ARG, "bytes_out is NULL");
+    int st = check_matrix_list(count, rows, cols);
+    if (st != DMUON_OK) return st;
+    if (backend != DMUON_NS_DIRECT && backend != DMUON_NS_GRAM) return fail(DMUON_ERR_INVALID_ARG, "bad backend");
+    PlanKey key;
+    key.kind = kPlanMuon;
+    key.backend = backend;
+    key.steps = 5;
+    key.restarts = {2};
+    key.rows.assign(rows, rows + count);
+    key.cols.assign(cols, cols + count);
+    Plan pl;
+    std::vector<const void*> G(count, nullptr);
+    std::vector<float*> Mo(count, nullptr), W(count, nullptr);
+    std::vector<void*> xo(count, nullptr);
+    st = build_plan_host(pl, key, G, Mo, W, xo);
+    if (st != DMUON_OK) return st;
+    *bytes_out = pl.bytes;
+    return DMUON_OK;
+  } catch (const std::exception& e) {
+    return fail(DMUON_ERR_OOM, "host exception: %s", e.what());
+  }
+}
+
+int dmuon_release_workspace(void) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  int dev = 0;
+  DM_CUDA(cudaGetDevice(&dev), "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return DMUON_OK;
+  DeviceState& ds = g_dev[dev];
+  if (ds.arena) {
+    DM_CUDA(cudaDeviceSynchronize(), "cudaDeviceSynchronize");
+    DM_CUDA(cudaFree(ds.arena), "cudaFree(workspace)");
+  }
+  ds.arena = nullptr;
+  ds.arena_bytes = 0;
+  ds.plan = Plan();
+  return DMUON_OK;
+}
+
+}  // extern "C"

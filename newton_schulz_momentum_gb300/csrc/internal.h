@@ -1,0 +1,123 @@
+// Internal types shared by the host layer (api.cu) and the kernels (gemm_tc.cu, rowwise.cu).
+// Nothing here is part of the public C ABI in include/dmuon.h.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace dmuon {
+
+// Bits of the device status word (read and cleared by dmuon_check_status).
+enum : unsigned {
+  kDevTimeout = 1u,    // a bounded mbarrier wait gave up; the launch's results are invalid
+  kDevNonfinite = 2u,  // an fp16 store overflowed or was NaN
+};
+
+// ------------------------------------------------------------------------------------------------
+// Grouped tensor-core GEMM (gemm_tc.cu).
+//
+// One launch processes a list of tiles drawn from a list of jobs; each job is one product
+// acc = A * Bop on one matrix, with its own operand tensor maps and epilogue. Tiles are 128 x BN
+// (BN = 128 or 256) output blocks with fp32 accumulators in tensor memory.
+// ------------------------------------------------------------------------------------------------
+
+constexpr int kBM = 128;  // tile rows (tcgen05 M)
+constexpr int kBK = 64;   // K per pipeline stage: 64 fp16 = one 128-byte swizzled row
+
+// How the epilogue forms v from the accumulator, the optional addend E and the step's (a, b, c).
+enum EpiRecipe : int {
+  kRecPlain = 0,   // v = acc
+  kRecZ = 1,       // v = c * acc + b * E          (Z = b R + c R^2; acc = R R, E = R)
+  kRecAxpy = 2,    // v = acc + a * E              (Z Q + a Q, Z R + a R, S Z + a S, B X + a X)
+  kRecCustom = 3,  // v = alpha * acc + beta * E + gamma * [i == j]
+};
+
+enum JobFlags : int {
+  kJobBMnMajor = 1,    // Bop is stored K x N (N contiguous): B tile loaded MN-major
+  kJobSymmetric = 2,   // upper-triangle tiles only; store D[i][j] and D[j][i] for j >= i
+  kJobFinal = 4,       // write fp32 W = w_alpha * W + w_beta * v instead of an fp16 D
+  kJobFinalTrans = 8,  // with kJobFinal: W is stored transposed (W[j][i])
+  kJobD2 = 16,         // also store D2 = v + a * [i == j] (the first Q after a (re)start)
+};
+
+struct alignas(128) GemmJob {
+  CUtensorMap tmA;  // A: M rows x K cols (K contiguous), box {64, 128}
+  CUtensorMap tmB;  // B: N x K (K contiguous) box {64, BN}, or K x N (N contiguous) box {64, 64}
+  __half* D;
+  __half* D2;
+  const __half* E;
+  float* W;
+  int64_t ldd, lde, ldw;  // leading dimensions in elements
+  int M, N, K;
+  int recipe, flags;
+  int tiles_n;  // number of BN-wide column tiles
+};
+static_assert(sizeof(GemmJob) % 128 == 0, "GemmJob must keep the tensor maps 128-byte aligned in arrays");
+
+struct GemmTile {
+  int job, tm, tn, pad_;
+};
+
+struct GemmLaunch {
+  // Either a device job table + tile list (grouped launch), or, when jobs == nullptr, the one job in
+  // `single` with tiles enumerated row-major over tiles_m x single.tiles_n.
+  GemmJob single;
+  const GemmJob* jobs;
+  const GemmTile* tiles;
+  int ntiles;
+  int tiles_m;
+  float a, b, c;             // this step's coefficients (recipes kRecZ / kRecAxpy / kJobD2)
+  float alpha, beta, gamma;  // kRecCustom
+  float w_alpha, w_beta;     // kJobFinal
+  unsigned* status;
+};
+
+// Launch one grouped GEMM (bn = 128 or 256) on `grid` persistent CTAs.
+cudaError_t launch_gemm(const GemmLaunch& p, int bn, int grid, cudaStream_t stream);
+// Dynamic shared memory each variant needs (host query).
+int gemm_smem_bytes(int bn);
+// Encode the operand tensor maps of a job (host). a/b point to fp16 row-major matrices.
+// b_mn_major selects the K x N storage of Bop. Returns false (with a message) on failure.
+bool encode_job_maps(GemmJob& job, const void* a, int64_t lda, const void* b, int64_t ldb,
+                     bool b_mn_major, int bn, const char** err);
+
+// ------------------------------------------------------------------------------------------------
+// Row-wise (HBM-bound) kernels (rowwise.cu): momentum + sum of squares, norm finalisation,
+// normalise + fp16 cast (+ transpose to the m <= n orientation).
+// ------------------------------------------------------------------------------------------------
+
+constexpr int kChunkElems = 65536;  // elements per momentum CTA (multiple of 8 * 256)
+constexpr int kCastTile = 64;       // normalise/cast tiles are 64 x 64 elements of M
+
+struct RowMat {
+  const void* G;  // gradient (fp32 or bf16), or null: M is only read
+  float* M;       // momentum, rows x cols fp32
+  __half* X;      // oriented fp16 output, m x n with leading dimension ldx
+  int64_t rows, cols, ldx;
+  int gdtype;     // 0 fp32, 1 bf16
+  int trans;      // rows > cols
+  int vec_ok;     // pointers and rows allow 16-byte vector access
+  int part_begin, part_count;  // this matrix's partial sums
+  int pad_;
+};
+
+struct RowLaunch {
+  const RowMat* mats;
+  int nmats;
+  const int64_t* chunk_prefix;  // nmats + 1 exclusive prefix of momentum chunks
+  const int64_t* tile_prefix;   // nmats + 1 exclusive prefix of 64 x 64 cast tiles
+  float* partials;              // one per chunk
+  float* norms;                 // one per matrix: ||M||_F
+  float* inv;                   // one per matrix: 1 / (||M||_F + eps)
+  float* norms_out;             // optional user copy of norms
+  float beta, eps;
+};
+
+cudaError_t launch_momentum_sumsq(const RowLaunch& p, int64_t nchunks, cudaStream_t stream);
+cudaError_t launch_finalize_norms(const RowLaunch& p, cudaStream_t stream);
+cudaError_t launch_normalize_cast(const RowLaunch& p, int64_t ntiles, cudaStream_t stream);
+
+}  // namespace dmuon

@@ -1,0 +1,241 @@
+// HBM-bound stages of the Muon update, grouped over all matrices of a call:
+//   1. momentum_sumsq   M <- beta * M + G and per-chunk partial sums of M^2 (pwwt.cn post, section 2:
+//                       keep a momentum of the gradient);
+//   2. finalize_norms   ||M||_F = sqrt(sum of partials) per matrix, in a fixed order, and
+//                       inv = 1 / (||M||_F + eps) ("Newton-Schulz 变体", section "精度流水线");
+//   3. normalize_cast   X = fp16(M * inv), written in the m <= n orientation (tall matrices are
+//                       transposed through shared memory) -- the fp16 input of the iteration.
+// Reductions are deterministic: fixed chunking, fixed tree order, no atomics.
+#include "internal.h"
+
+namespace dmuon {
+namespace {
+
+constexpr int kThreads = 256;
+
+// Index of the matrix whose [prefix[i], prefix[i+1]) range holds `item`.
+__device__ __forceinline__ int find_matrix(const int64_t* prefix, int n, int64_t item) {
+  int lo = 0, hi = n;  // prefix[lo] <= item < prefix[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (prefix[mid] <= item) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+__device__ __forceinline__ void load8_grad(const void* g, int gdtype, int64_t e, float (&out)[8]) {
+  if (gdtype == 1) {
+    const uint4 u = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(g) + e));
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      out[2 * k] = __uint_as_float(w[k] << 16);
+      out[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+    }
+  } else {
+    const float4 a = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(g) + e));
+    const float4 b = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(g) + e + 4));
+    out[0] = a.x; out[1] = a.y; out[2] = a.z; out[3] = a.w;
+    out[4] = b.x; out[5] = b.y; out[6] = b.z; out[7] = b.w;
+  }
+}
+
+__device__ __forceinline__ float load1_grad(const void* g, int gdtype, int64_t e) {
+  if (gdtype == 1) return __uint_as_float(static_cast<uint32_t>(static_cast<const uint16_t*>(g)[e]) << 16);
+  return static_cast<const float*>(g)[e];
+}
+
+template <typename T>
+__device__ __forceinline__ T block_sum(T v, T* scratch) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) scratch[warp] = v;
+  __syncthreads();
+  T total = 0;
+  if (threadIdx.x == 0) {
+    for (int w = 0; w < kThreads / 32; ++w) total += scratch[w];
+  }
+  return total;  // valid in thread 0
+}
+
+__global__ void __launch_bounds__(kThreads) momentum_sumsq_kernel(const RowLaunch p) {
+  __shared__ float red[kThreads / 32];
+  const int64_t chunk = blockIdx.x;
+  const int mi = find_matrix(p.chunk_prefix, p.nmats, chunk);
+  const RowMat mt = p.mats[mi];
+  const int64_t local = chunk - p.chunk_prefix[mi];
+  const int64_t numel = mt.rows * mt.cols;
+  const int64_t begin = local * kChunkElems;
+  const int64_t end = min(begin + static_cast<int64_t>(kChunkElems), numel);
+  const bool has_g = mt.G != nullptr;
+  const float beta = p.beta;
+  float acc = 0.f;
+  int64_t scalar_from = begin;
+  if (mt.vec_ok) {
+    const int64_t vend = begin + ((end - begin) / 8) * 8;
+    // 4 groups of 8 elements in flight per thread.
+    int64_t e = begin + threadIdx.x * 8;
+    for (; e + 3 * kThreads * 8 + 8 <= vend; e += 4 * kThreads * 8) {
+      float g[4][8];
+      float4 m[4][2];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int64_t eu = e + u * kThreads * 8;
+        if (has_g) load8_grad(mt.G, mt.gdtype, eu, g[u]);
+        m[u][0] = *reinterpret_cast<const float4*>(mt.M + eu);
+        m[u][1] = *reinterpret_cast<const float4*>(mt.M + eu + 4);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        float* mv = reinterpret_cast<float*>(m[u]);
+        if (has_g) {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) mv[k] = fmaf(beta, mv[k], g[u][k]);
+          const int64_t eu = e + u * kThreads * 8;
+          *reinterpret_cast<float4*>(mt.M + eu) = m[u][0];
+          *reinterpret_cast<float4*>(mt.M + eu + 4) = m[u][1];
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) acc = fmaf(mv[k], mv[k], acc);
+      }
+    }
+    for (; e + 8 <= vend; e += kThreads * 8) {
+      float g[8];
+      float4 m[2];
+      if (has_g) load8_grad(mt.G, mt.gdtype, e, g);
+      m[0] = *reinterpret_cast<const float4*>(mt.M + e);
+      m[1] = *reinterpret_cast<const float4*>(mt.M + e + 4);
+      float* mv = reinterpret_cast<float*>(m);
+      if (has_g) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mv[k] = fmaf(beta, mv[k], g[k]);
+        *reinterpret_cast<float4*>(mt.M + e) = m[0];
+        *reinterpret_cast<float4*>(mt.M + e + 4) = m[1];
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k) acc = fmaf(mv[k], mv[k], acc);
+    }
+    scalar_from = vend;
+  }
+  for (int64_t e = scalar_from + threadIdx.x; e < end; e += kThreads) {
+    float m = mt.M[e];
+    if (has_g) {
+      m = fmaf(beta, m, load1_grad(mt.G, mt.gdtype, e));
+      mt.M[e] = m;
+    }
+    acc = fmaf(m, m, acc);
+  }
+  const float total = block_sum(acc, red);
+  if (threadIdx.x == 0) p.partials[mt.part_begin + local] = total;
+}
+
+__global__ void __launch_bounds__(kThreads) finalize_norms_kernel(const RowLaunch p) {
+  __shared__ double red[kThreads / 32];
+  const RowMat mt = p.mats[blockIdx.x];
+  double s = 0.0;
+  for (int k = threadIdx.x; k < mt.part_count; k += kThreads) s += static_cast<double>(p.partials[mt.part_begin + k]);
+  const double total = block_sum(s, red);
+  if (threadIdx.x == 0) {
+    const double norm = sqrt(total);
+    p.norms[blockIdx.x] = static_cast<float>(norm);
+    p.inv[blockIdx.x] = static_cast<float>(1.0 / (norm + static_cast<double>(p.eps)));
+    if (p.norms_out) p.norms_out[blockIdx.x] = static_cast<float>(norm);
+  }
+}
+
+__device__ __forceinline__ void store_half4(__half* dst, float a, float b, float c, float d) {
+  __half2 lo = __floats2half2_rn(a, b), hi = __floats2half2_rn(c, d);
+  uint2 u;
+  u.x = *reinterpret_cast<uint32_t*>(&lo);
+  u.y = *reinterpret_cast<uint32_t*>(&hi);
+  *reinterpret_cast<uint2*>(dst) = u;
+}
+
+__global__ void __launch_bounds__(kThreads) normalize_cast_kernel(const RowLaunch p) {
+  __shared__ float tile[kCastTile][kCastTile + 1];
+  const int64_t t = blockIdx.x;
+  const int mi = find_matrix(p.tile_prefix, p.nmats, t);
+  const RowMat mt = p.mats[mi];
+  const int64_t local = t - p.tile_prefix[mi];
+  const int64_t tiles_c = (mt.cols + kCastTile - 1) / kCastTile;
+  const int64_t r0 = (local / tiles_c) * kCastTile;
+  const int64_t c0 = (local % tiles_c) * kCastTile;
+  const float inv = p.inv[mi];
+  const bool vec = mt.vec_ok && (mt.cols & 3) == 0;
+  const int tx = threadIdx.x & 15;   // 4-column group within the tile
+  const int ty = threadIdx.x >> 4;   // row within a 16-row pass
+
+  if (!mt.trans) {
+    for (int pass = 0; pass < kCastTile / 16; ++pass) {
+      const int64_t r = r0 + pass * 16 + ty;
+      const int64_t c = c0 + tx * 4;
+      if (r >= mt.rows) continue;
+      const float* src = mt.M + r * mt.cols + c;
+      __half* dst = mt.X + r * mt.ldx + c;
+      if (vec && c + 4 <= mt.cols) {
+        const float4 v = *reinterpret_cast<const float4*>(src);
+        store_half4(dst, v.x * inv, v.y * inv, v.z * inv, v.w * inv);
+      } else {
+        for (int k = 0; k < 4; ++k)
+          if (c + k < mt.cols) dst[k] = __float2half_rn(src[k] * inv);
+      }
+    }
+    return;
+  }
+
+  // Tall matrix: X (cols x rows) = (M * inv)^T.
+  for (int pass = 0; pass < kCastTile / 16; ++pass) {
+    const int rr = pass * 16 + ty;
+    const int64_t r = r0 + rr;
+    const int64_t c = c0 + tx * 4;
+    if (r >= mt.rows) continue;
+    const float* src = mt.M + r * mt.cols + c;
+    if (vec && c + 4 <= mt.cols) {
+      const float4 v = *reinterpret_cast<const float4*>(src);
+      tile[rr][tx * 4 + 0] = v.x;
+      tile[rr][tx * 4 + 1] = v.y;
+      tile[rr][tx * 4 + 2] = v.z;
+      tile[rr][tx * 4 + 3] = v.w;
+    } else {
+      for (int k = 0; k < 4; ++k)
+        if (c + k < mt.cols) tile[rr][tx * 4 + k] = src[k];
+    }
+  }
+  __syncthreads();
+  for (int pass = 0; pass < kCastTile / 16; ++pass) {
+    const int cc = pass * 16 + ty;      // row of X (column of M)
+    const int rr = tx * 4;              // first of 4 consecutive columns of X (rows of M)
+    const int64_t xr = c0 + cc;
+    const int64_t xc = r0 + rr;
+    if (xr >= mt.cols) continue;
+    __half* dst = mt.X + xr * mt.ldx + xc;
+    if (xc + 4 <= mt.rows) {
+      store_half4(dst, tile[rr][cc] * inv, tile[rr + 1][cc] * inv, tile[rr + 2][cc] * inv, tile[rr + 3][cc] * inv);
+    } else {
+      for (int k = 0; k < 4; ++k)
+        if (xc + k < mt.rows) dst[k] = __float2half_rn(tile[rr + k][cc] * inv);
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_momentum_sumsq(const RowLaunch& p, int64_t nchunks, cudaStream_t stream) {
+  if (nchunks <= 0) return cudaSuccess;
+  momentum_sumsq_kernel<<<static_cast<unsigned>(nchunks), kThreads, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_finalize_norms(const RowLaunch& p, cudaStream_t stream) {
+  finalize_norms_kernel<<<p.nmats, kThreads, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_normalize_cast(const RowLaunch& p, int64_t ntiles, cudaStream_t stream) {
+  if (ntiles <= 0) return cudaSuccess;
+  normalize_cast_kernel<<<static_cast<unsigned>(ntiles), kThreads, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace dmuon

@@ -1,0 +1,113 @@
+"""CPU checks of the C ABI and the binding: the library loads without a GPU, exports exactly what
+include/dmuon.h declares, rejects bad arguments before touching a device, and its host-side planning
+and flop accounting agree with closed forms."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import newton_schulz_momentum_gb300 as dm
+from newton_schulz_momentum_gb300 import build as dmbuild
+from tests import _pins
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    dmbuild.build()
+    return dm.lib()
+
+
+def header_functions():
+    src = open(os.path.join(ROOT, "include", "dmuon.h")).read()
+    return sorted(set(re.findall(r"DMUON_API\s+[\w\s\*]+?\b(dmuon_\w+)\s*\(", src)))
+
+
+def test_exports_match_header(L):
+    declared = header_functions()
+    assert declared, "no declarations found in include/dmuon.h"
+    assert sorted(dm.EXPORTS) == declared
+    for name in declared:
+        assert hasattr(L, name), name
+    out = os.popen(f"nm -D --defined-only {dm.LIB_PATH}").read()
+    exported = sorted(set(re.findall(r" T (dmuon_\w+)", out)))
+    assert exported == declared
+
+
+def test_version(L):
+    assert dm.version().startswith("dmuon-gb300")
+
+
+def test_tables_match_pages():
+    g = _pins.golden_coefficients()
+    assert dm.POLAR_EXPRESS == g["POLAR_EXPRESS"]
+    assert dm.YOU == g["YOU"]
+
+
+def _status(L, rc):
+    return rc, L.dmuon_last_error().decode()
+
+
+def test_invalid_arguments_rejected_without_device(L):
+    c = (ctypes.c_float * 15)(*[1.0] * 15)
+    r = (ctypes.c_int * 1)(2)
+    rc, msg = _status(L, L.dmuon_ns(None, 4, 8, c, 5, r, 1, 1, 1e-7, None))
+    assert rc == dm.ERR_INVALID_ARG and "NULL" in msg
+    rc, msg = _status(L, L.dmuon_ns(4096, 4, 8, c, 5, r, 1, 7, 1e-7, None))
+    assert rc == dm.ERR_INVALID_ARG and "backend" in msg
+    rc, msg = _status(L, L.dmuon_ns(4096, 4, 8, c, 0, r, 1, 1, 1e-7, None))
+    assert rc == dm.ERR_INVALID_ARG and "steps" in msg
+    bad = (ctypes.c_int * 2)(3, 2)
+    rc, msg = _status(L, L.dmuon_ns(4096, 4, 8, c, 5, bad, 2, 1, 1e-7, None))
+    assert rc == dm.ERR_INVALID_ARG and "increasing" in msg
+    out = (ctypes.c_int * 1)(5)
+    rc, msg = _status(L, L.dmuon_ns(4096, 4, 8, c, 5, out, 1, 1, 1e-7, None))
+    assert rc == dm.ERR_INVALID_ARG and "restart" in msg
+    rc, msg = _status(L, L.dmuon_ns(4096, 0, 8, c, 5, r, 1, 1, 1e-7, None))
+    assert rc == dm.ERR_INVALID_ARG
+    rc, msg = _status(L, L.dmuon_ns(4100, 4, 8, c, 5, r, 1, 1, 1e-7, None))
+    assert rc == dm.ERR_INVALID_ARG and "aligned" in msg
+    rc, msg = _status(L, L.dmuon_ns(4096, 4, 8, c, 5, r, 1, 1, -1.0, None))
+    assert rc == dm.ERR_INVALID_ARG and "eps" in msg
+    nan = (ctypes.c_float * 15)(*([float("nan")] + [1.0] * 14))
+    rc, msg = _status(L, L.dmuon_ns(4096, 4, 8, nan, 5, r, 1, 1, 1e-7, None))
+    assert rc == dm.ERR_INVALID_ARG and "finite" in msg
+    # GEMM building block
+    rc, msg = _status(L, L.dmuon_gemm_f16(8, 9, 16, 4096, 16, 4096, 16, 1, None, 0, 4096, 16, 1.0, 0.0, 0.0, 1, None))
+    assert rc == dm.ERR_INVALID_ARG and "M == N" in msg
+    rc, msg = _status(L, L.dmuon_gemm_f16(8, 8, 16, 4096, 12, 4096, 16, 1, None, 0, 4096, 16, 1.0, 0.0, 0.0, 0, None))
+    assert rc == dm.ERR_INVALID_ARG and "leading" in msg
+    rc, msg = _status(L, L.dmuon_gemm_f16(8, 8, 16, 4096, 20, 4096, 16, 1, None, 0, 4096, 16, 1.0, 0.0, 0.0, 0, None))
+    assert rc == dm.ERR_INVALID_ARG and "multiples of 8" in msg
+    # batched step
+    P = (ctypes.c_void_p * 1)(4096)
+    rows = (ctypes.c_int64 * 1)(4)
+    cols = (ctypes.c_int64 * 1)(8)
+    rc, msg = _status(L, L.dmuon_muon_step(1, P, P, 3, P, rows, cols, None, 0.02, 0.95, c, 5, r, 1, 1, 1e-7, None))
+    assert rc == dm.ERR_INVALID_ARG and "grad_dtype" in msg
+    rc, msg = _status(L, L.dmuon_muon_step(0, P, P, 0, P, rows, cols, None, 0.02, 0.95, c, 5, r, 1, 1, 1e-7, None))
+    assert rc == dm.ERR_INVALID_ARG and "count" in msg
+
+
+def test_flop_counts_closed_form():
+    for m, n in ((4096, 4096), (1024, 4096), (4096, 14336), (128, 512), (7, 3)):
+        mm, nn = min(m, n), max(m, n)
+        assert dm.gram_flops(m, n) == 6 * mm * mm * nn + 20 * mm ** 3
+        assert dm.direct_flops(m, n) == 15 * mm * mm * nn + 5 * mm ** 3
+    # no restart: X X^T + 5 R^2 + 4 Q updates + 4 R updates + output
+    assert dm.gram_flops(10, 20, 5, ()) == 100 * 20 + 5 * 1000 + 4 * 2000 + 4 * 3000 + 2 * 100 * 20
+
+
+def test_workspace_size_closed_form(L):
+    # Gram: two fp16 X buffers (m x roundup(n, 8)) and five fp16 m x roundup(m, 8) buffers per matrix,
+    # plus small tables. Direct: two X buffers and two m x m buffers.
+    shapes = [(4096, 4096), (1024, 4096), (14336, 4096), (4096, 14336)]
+    big = sum(2 * 2 * min(s) * max(s) + 5 * 2 * min(s) ** 2 for s in shapes)
+    got = dm.workspace_size(shapes, "gram")
+    assert big <= got <= big * 1.001 + (1 << 22)
+    small = sum(2 * 2 * min(s) * max(s) + 2 * 2 * min(s) ** 2 for s in shapes)
+    got = dm.workspace_size(shapes, "direct")
+    assert small <= got <= small * 1.001 + (1 << 22)
