@@ -1,0 +1,348 @@
+"""Benchmark: one owner-rank Muon step over the Muon-target matrices of a Llama-3-8B-shaped model.
+
+A step is the whole path on every matrix: momentum accumulate (bf16 gradients, fp32 momentum), fp32
+Frobenius normalisation, fp16 cast, five Newton-Schulz steps (Gram form with restart [2] by default,
+POLAR_EXPRESS coefficients) and the fp32 weight update -- one dmuon_muon_step call.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--backend gram|direct] [--layers L]
+    python bench.py --impl reference ...   # the CPU float64 oracle on a bounded sample
+
+value = algorithmic Newton-Schulz TFLOP/s of the whole job (symmetric products at half: Gram
+6 m^2 n + 20 m^3 per matrix, direct 15 m^2 n + 5 m^3) over the device-timed region, inputs resident in
+HBM. Every input is larger than L2 (129 MB) except the small Gram matrices, so no flush is inserted.
+e2e = the same metric through the public call with the step's gradients copied in from pinned host
+memory and the per-matrix norms read back, inside the timed region.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "Muon NS step ms & TFLOP/s (frac of fp16 tensor peak), 8B Llama matrix set"
+UNIT = "TFLOP/s"
+LR, BETA, EPS = 0.02, 0.95, 1e-7
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--backend", default="gram", choices=["gram", "direct"])
+    ap.add_argument("--layers", type=int, default=32)
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline (profiling runs)")
+    return ap.parse_args()
+
+
+def workload_config(args):
+    import workloads
+    shapes = workloads.llama3_8b_shapes(args.layers)
+    return shapes, {
+        "workload": f"llama3-8b-muon-set-{args.layers}L" if args.layers != 32 else "llama3-8b-muon-set",
+        "matrices": len(shapes),
+        "params": sum(r * c for _, r, c in shapes),
+        "shapes": "per layer q/o 4096x4096, k/v 1024x4096, gate/up 14336x4096, down 4096x14336",
+        "grad_dtype": "bf16", "state_dtype": "fp32", "backend": args.backend,
+        "coefficients": "POLAR_EXPRESS", "restarts": [2] if args.backend == "gram" else [],
+        "lr": LR, "beta": BETA, "eps": EPS,
+        "l2": "inputs larger than L2, no flush",
+    }
+
+
+def total_flops(shapes, backend):
+    import newton_schulz_momentum_gb300 as dm
+    f = dm.gram_flops if backend == "gram" else dm.direct_flops
+    return sum(f(r, c) for _, r, c in shapes)
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
+            p = json.load(fh)
+        return p["hbm_gbs"], p["bf16_tflops"], p["bf16_tflops_sustained"], "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples every 200 ms while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in getattr(self, "lines", []):
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def cpu_oracle_sample(shapes, backend, seconds, seed=7):
+    """Time the float64 oracle (as it stands) on whole matrices of the workload's distinct oriented
+    shapes, cycling until about `seconds` of CPU work. Returns (TFLOP/s, flops, seconds, sample text)."""
+    import numpy as np
+
+    import newton_schulz_momentum_gb300 as dm
+    import workloads
+    from oracle import ns64
+
+    distinct = []
+    for name, r, c in shapes:
+        key = (min(r, c), max(r, c))
+        if key not in [(min(a, b), max(a, b)) for _, a, b in distinct]:
+            distinct.append((name, r, c))
+    distinct.sort(key=lambda t: t[1] * t[2])
+    flops, spent, done = 0, 0.0, []
+    i = 0
+    while spent < seconds or not done:
+        name, r, c = distinct[i % len(distinct)]
+        g = workloads.round_to_bf16(workloads.gaussian((r, c), 1e-3, seed + i))[0]
+        w = workloads.gaussian((r, c), 0.02, seed + 100 + i)
+        m0 = np.zeros((r, c), dtype=np.float32)
+        t0 = time.perf_counter()
+        ns64.muon_step(w, g, m0, LR, BETA, ns64.POLAR_EXPRESS, (2,) if backend == "gram" else (), backend, EPS)
+        spent += time.perf_counter() - t0
+        flops += (dm.gram_flops if backend == "gram" else dm.direct_flops)(r, c)
+        done.append(f"{name.split('.')[-1]} {r}x{c}")
+        i += 1
+        if i >= 3 * len(distinct):
+            break
+    return flops / spent / 1e12, flops, spent, "whole-matrix oracle Muon steps: " + ", ".join(done)
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def run_reference(args):
+    """--impl reference: the CPU float64 oracle on the same workload, metric and unit."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    shapes, cfg = workload_config(args)
+    per_step = max(args.cpu_seconds / 4.0, 1.0)
+    for _ in range(args.warmup):
+        cpu_oracle_sample(shapes[:7], args.backend, 0.0)
+    tflops, flops, secs = [], 0, 0.0
+    sample = ""
+    for _ in range(args.steps):
+        v, f, s, sample = cpu_oracle_sample(shapes[:7], args.backend, per_step)
+        tflops.append(v)
+        flops += f
+        secs += s
+    value = flops / secs / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": cfg,
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
+                         "sample": f"per step about {per_step:.0f} s of {sample}"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_e2e(args, G, norms, step, barrier, stream, world, flops_step):
+    """Same metric through the public call, with each step's gradients copied in from pinned host memory
+    and the per-matrix norms (the step's reported result) read back, all inside the timed region."""
+    import torch
+    import torch.distributed as dist
+
+    host_g = [g.cpu().pin_memory() for g in G]
+    host_norms = torch.empty(norms.numel(), dtype=torch.float32).pin_memory()
+    h2d = sum(g.numel() * g.element_size() for g in host_g)
+    d2h = host_norms.numel() * host_norms.element_size()
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    start.record(stream)
+    for _ in range(args.e2e_steps):
+        for gd, gh in zip(G, host_g):
+            gd.copy_(gh, non_blocking=True)
+        step()
+        host_norms.copy_(norms, non_blocking=True)
+    stop.record(stream)
+    barrier()
+    ms = start.elapsed_time(stop)
+    if world > 1:
+        t = torch.tensor([ms], device=norms.device, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    del host_g
+    return {"value": world * flops_step / (ms / args.e2e_steps * 1e-3) / 1e12, "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms / args.e2e_steps}
+
+
+def run_native(args):
+    import torch
+    import torch.distributed as dist
+
+    import newton_schulz_momentum_gb300 as dm
+    from newton_schulz_momentum_gb300 import build as dmbuild
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world != args.gpus:
+        raise SystemExit(f"--gpus {args.gpus} but WORLD_SIZE={world}")
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl")
+    dmbuild.build()
+    dm.lib()
+
+    shapes, cfg = workload_config(args)
+    flops_step = total_flops(shapes, args.backend)
+    dev = torch.device("cuda", local)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(1234 + rank)
+    W, G, M = [], [], []
+    for _, r, c in shapes:
+        W.append(torch.randn((r, c), generator=gen, device=dev) * 0.02)
+        G.append((torch.randn((r, c), generator=gen, device=dev) * 1e-3).to(torch.bfloat16))
+        M.append(torch.zeros((r, c), dtype=torch.float32, device=dev))
+    norms = torch.empty(len(shapes), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        dm.muon_step(W, G, M, lr=LR, beta=BETA, coeffs=dm.POLAR_EXPRESS, restarts=(2,), backend=args.backend,
+                     eps=EPS, norms_out=norms, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    dm.check_status(stream)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    # ---- device-resident timed region
+    dm.timing_enable(True)
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    with ClockSampler(local) as clocks:
+        start.record(stream)
+        for _ in range(args.steps):
+            step()
+        stop.record(stream)
+        barrier()
+    ms = start.elapsed_time(stop)
+    kernel_times = dm.timing_read()
+    dm.timing_enable(False)
+    dm.check_status(stream)
+    if world > 1:
+        t = torch.tensor([ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_step = ms / args.steps
+    value = world * flops_step / (ms_step * 1e-3) / 1e12
+
+    # ---- end to end through the public call: pinned host gradients in, norms out
+    e2e = None
+    if args.e2e_steps > 0:
+        e2e = run_e2e(args, G, norms, step, barrier, stream, world, flops_step)
+
+    # ---- roofline of the dominant kernel (the tensor-core GEMM), from the live events
+    hbm, tc_burst, tc_sust, src = peaks()
+    gemm_ms, gemm_n = kernel_times["gemm_tc"]
+    per_launch_flops = flops_step * args.steps / max(gemm_n, 1)
+    achieved = per_launch_flops / (gemm_ms / max(gemm_n, 1) * 1e-3) / 1e12 if gemm_ms > 0 else None
+    launches = sum(n for _, n in kernel_times.values())
+    rw_ms = sum(kernel_times[k][0] for k in ("momentum_sumsq", "finalize_norms", "normalize_cast"))
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        v, f, s, sample = cpu_oracle_sample(shapes, args.backend, args.cpu_seconds)
+        cpu = {"value": v, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
+               "sample": f"{sample} ({f / 1e12:.2f} TFLOP in {s:.1f} s, float64 NumPy)"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f16", "data": "synthetic", "config": cfg,
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": tc_sust, "unit": "TFLOP/s",
+                         "frac": (achieved / tc_sust) if achieved else None, "traffic": None,
+                         "kernel": "gemm_tc_kernel (tcgen05 fp16, fp32 accumulate)",
+                         "peak_source": f"{src} bf16 sustained (fp16 dense rate equals bf16)"},
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": launches,
+            "clocks": clocks.summary(),
+            "breakdown_ms_per_step": {k: v[0] / args.steps for k, v in kernel_times.items()},
+            "launches_per_step": {k: v[1] / args.steps for k, v in kernel_times.items()},
+            "rowwise_hbm": {"bytes_per_step": sum(r * c for _, r, c in shapes) * 16,
+                            "achieved_gbs": (sum(r * c for _, r, c in shapes) * 16 * args.steps / (rw_ms * 1e-3) / 1e9)
+                            if rw_ms > 0 else None, "peak_gbs": hbm},
+            "ns_tflops_frac_of_peak": value / world / tc_sust,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_native(args)
+
+
+if __name__ == "__main__":
+    main()

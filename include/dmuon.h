@@ -154,6 +154,18 @@ DMUON_API int dmuon_gemm_f16(int64_t M, int64_t N, int64_t K, const void* A, int
  */
 DMUON_API int dmuon_check_status(void* cuda_stream);
 
+/*
+ * Per-kernel CUDA-event timing (off by default; used by benchmarks). While enabled, the library records
+ * a pair of CUDA events on the caller's stream around every kernel it launches. dmuon_timing_read
+ * waits for the recorded events, writes per kernel class the summed elapsed milliseconds and the
+ * number of launches since the previous read (or enable), and clears the record. Classes:
+ *   0 momentum + sum of squares, 1 norm finalisation, 2 normalise + fp16 cast, 3 tensor-core GEMM.
+ * ms_out and launches_out must each hold DMUON_TIMING_CLASSES entries (host memory).
+ */
+#define DMUON_TIMING_CLASSES 4
+DMUON_API int dmuon_timing_enable(int on);
+DMUON_API int dmuon_timing_read(double* ms_out, int64_t* launches_out);
+
 /* Text of the last error on the calling thread; valid until the next call on that thread. */
 DMUON_API const char* dmuon_last_error(void);
 

@@ -43,8 +43,9 @@ F32, BF16 = 0, 1
 EXPORTS = (
     "dmuon_ns", "dmuon_muon_step", "dmuon_momentum_normalize", "dmuon_gemm_f16", "dmuon_check_status",
     "dmuon_last_error", "dmuon_version", "dmuon_set_workspace_limit", "dmuon_workspace_size",
-    "dmuon_release_workspace",
+    "dmuon_release_workspace", "dmuon_timing_enable", "dmuon_timing_read",
 )
+TIMING_CLASSES = ("momentum_sumsq", "finalize_norms", "normalize_cast", "gemm_tc")
 
 
 class LibraryNotBuilt(RuntimeError):
@@ -84,6 +85,8 @@ def lib():
     L.dmuon_version.restype = ctypes.c_char_p
     L.dmuon_set_workspace_limit.argtypes = [ctypes.c_size_t]
     L.dmuon_workspace_size.argtypes = [i32, _c_i64p, _c_i64p, i32, ctypes.POINTER(ctypes.c_size_t)]
+    L.dmuon_timing_enable.argtypes = [i32]
+    L.dmuon_timing_read.argtypes = [ctypes.POINTER(ctypes.c_double), _c_i64p]
     for name in EXPORTS:
         if name not in ("dmuon_last_error", "dmuon_version"):
             getattr(L, name).restype = ctypes.c_int
@@ -218,6 +221,19 @@ def workspace_size(shapes, backend="gram"):
     out = ctypes.c_size_t(0)
     _check(lib().dmuon_workspace_size(n, rows, cols, _backend(backend), ctypes.byref(out)))
     return out.value
+
+
+def timing_enable(on=True):
+    """Record CUDA events around every library launch (on the launching stream) until disabled."""
+    _check(lib().dmuon_timing_enable(1 if on else 0))
+
+
+def timing_read():
+    """{class: (milliseconds, launches)} since the last read; waits for the recorded events."""
+    ms = (ctypes.c_double * len(TIMING_CLASSES))()
+    n = (ctypes.c_int64 * len(TIMING_CLASSES))()
+    _check(lib().dmuon_timing_read(ms, n))
+    return {c: (ms[i], n[i]) for i, c in enumerate(TIMING_CLASSES)}
 
 
 def release_workspace():

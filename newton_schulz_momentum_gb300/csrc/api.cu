@@ -132,6 +132,46 @@ struct DeviceState {
 
 std::mutex g_mu;
 constexpr int kMaxDevices = 64;
+
+// Opt-in event timing (dmuon_timing_enable / dmuon_timing_read).
+struct TimedLaunch {
+  int cls;
+  cudaEvent_t start, stop;
+};
+bool g_timing = false;
+std::vector<TimedLaunch> g_timed;
+std::vector<cudaEvent_t> g_event_pool;
+
+cudaEvent_t take_event() {
+  if (!g_event_pool.empty()) {
+    cudaEvent_t e = g_event_pool.back();
+    g_event_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  return e;
+}
+
+// Records events around one launch when timing is on; otherwise just launches.
+template <typename F>
+cudaError_t timed(int cls, cudaStream_t stream, F&& launch) {
+  if (!g_timing) return launch();
+  cudaEvent_t a = take_event(), b = take_event();
+  if (a) cudaEventRecord(a, stream);
+  const cudaError_t e = launch();
+  if (b) cudaEventRecord(b, stream);
+  if (a && b) {
+    g_timed.push_back({cls, a, b});
+  } else {
+    if (a) g_event_pool.push_back(a);
+    if (b) g_event_pool.push_back(b);
+  }
+  return e;
+}
 DeviceState g_dev[kMaxDevices];
 size_t g_ws_limit = 0;
 
@@ -513,9 +553,10 @@ int run_plan(DeviceState& ds, const Plan& pl, const float* coeffs, float lr, flo
   rl.norms_out = norms_out;
   rl.beta = beta;
   rl.eps = eps;
-  DM_CUDA(launch_momentum_sumsq(rl, pl.nchunks, stream), "momentum/sum-of-squares launch");
-  DM_CUDA(launch_finalize_norms(rl, stream), "norm launch");
-  DM_CUDA(launch_normalize_cast(rl, pl.ncast, stream), "normalise/cast launch");
+  DM_CUDA(timed(0, stream, [&] { return launch_momentum_sumsq(rl, pl.nchunks, stream); }),
+          "momentum/sum-of-squares launch");
+  DM_CUDA(timed(1, stream, [&] { return launch_finalize_norms(rl, stream); }), "norm launch");
+  DM_CUDA(timed(2, stream, [&] { return launch_normalize_cast(rl, pl.ncast, stream); }), "normalise/cast launch");
   const GemmJob* jobs = reinterpret_cast<const GemmJob*>(base + pl.off_jobs);
   const GemmTile* tiles = reinterpret_cast<const GemmTile*>(base + pl.off_tiles);
   for (const LaunchRec& L : pl.launches) {
@@ -531,7 +572,7 @@ int run_plan(DeviceState& ds, const Plan& pl, const float* coeffs, float lr, flo
     gl.w_beta = pl.key.kind == kPlanNs ? 1.f : -lr;
     gl.status = ds.status;
     const int grid = std::min(L.ntiles, ds.sms);
-    DM_CUDA(launch_gemm(gl, L.bn, grid, stream), "tensor-core GEMM launch");
+    DM_CUDA(timed(3, stream, [&] { return launch_gemm(gl, L.bn, grid, stream); }), "tensor-core GEMM launch");
   }
   return DMUON_OK;
 }
@@ -727,7 +768,8 @@ int dmuon_gemm_f16(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, 
     gl.alpha = alpha, gl.beta = E ? beta : 0.f, gl.gamma = gamma;
     gl.status = ds->status;
     const int grid = static_cast<int>(std::min<int64_t>(ntiles, ds->sms));
-    DM_CUDA(launch_gemm(gl, bn, grid, static_cast<cudaStream_t>(cuda_stream)), "tensor-core GEMM launch");
+    cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
+    DM_CUDA(timed(3, stream, [&] { return launch_gemm(gl, bn, grid, stream); }), "tensor-core GEMM launch");
     return DMUON_OK;
   } catch (const std::exception& e) {
     return fail(DMUON_ERR_OOM, "host exception: %s", e.what());
@@ -746,6 +788,39 @@ int dmuon_check_status(void* cuda_stream) {
   if (word & kDevTimeout) return fail(DMUON_ERR_TIMEOUT, "a device-side bounded wait gave up; results are invalid");
   if (word & kDevNonfinite) return fail(DMUON_ERR_NONFINITE, "an fp16 intermediate overflowed or was NaN");
   return DMUON_OK;
+}
+
+int dmuon_timing_enable(int on) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  for (auto& t : g_timed) {
+    cudaEventSynchronize(t.stop);
+    g_event_pool.push_back(t.start);
+    g_event_pool.push_back(t.stop);
+  }
+  g_timed.clear();
+  g_timing = on != 0;
+  return DMUON_OK;
+}
+
+int dmuon_timing_read(double* ms_out, int64_t* launches_out) {
+  if (!ms_out || !launches_out) return fail(DMUON_ERR_INVALID_ARG, "output arrays are NULL");
+  std::lock_guard<std::mutex> lock(g_mu);
+  for (int c = 0; c < DMUON_TIMING_CLASSES; ++c) ms_out[c] = 0.0, launches_out[c] = 0;
+  int st = DMUON_OK;
+  for (auto& t : g_timed) {
+    float ms = 0.f;
+    cudaError_t e = cudaEventSynchronize(t.stop);
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, t.start, t.stop);
+    if (e != cudaSuccess && st == DMUON_OK) st = cuda_fail(e, "timing events");
+    if (t.cls >= 0 && t.cls < DMUON_TIMING_CLASSES) {
+      ms_out[t.cls] += ms;
+      launches_out[t.cls] += 1;
+    }
+    g_event_pool.push_back(t.start);
+    g_event_pool.push_back(t.stop);
+  }
+  g_timed.clear();
+  return st;
 }
 
 const char* dmuon_last_error(void) { return t_last_error.c_str(); }

@@ -162,7 +162,10 @@ __global__ void __launch_bounds__(kThreads) normalize_cast_kernel(const RowLaunc
   const int64_t r0 = (local / tiles_c) * kCastTile;
   const int64_t c0 = (local % tiles_c) * kCastTile;
   const float inv = p.inv[mi];
-  const bool vec = mt.vec_ok && (mt.cols & 3) == 0;
+  // 16-byte loads of M need rows of a multiple of 4 floats; 8-byte stores of X need rows of X
+  // (ldx halves) of a multiple of 4. Either condition failing falls back to scalar accesses.
+  const bool vec_in = mt.vec_ok && (mt.cols & 3) == 0;
+  const bool vec_out = (mt.ldx & 3) == 0 && (reinterpret_cast<uintptr_t>(mt.X) & 7) == 0;
   const int tx = threadIdx.x & 15;   // 4-column group within the tile
   const int ty = threadIdx.x >> 4;   // row within a 16-row pass
 
@@ -173,7 +176,7 @@ __global__ void __launch_bounds__(kThreads) normalize_cast_kernel(const RowLaunc
       if (r >= mt.rows) continue;
       const float* src = mt.M + r * mt.cols + c;
       __half* dst = mt.X + r * mt.ldx + c;
-      if (vec && c + 4 <= mt.cols) {
+      if (vec_in && vec_out && c + 4 <= mt.cols) {
         const float4 v = *reinterpret_cast<const float4*>(src);
         store_half4(dst, v.x * inv, v.y * inv, v.z * inv, v.w * inv);
       } else {
@@ -191,7 +194,7 @@ __global__ void __launch_bounds__(kThreads) normalize_cast_kernel(const RowLaunc
     const int64_t c = c0 + tx * 4;
     if (r >= mt.rows) continue;
     const float* src = mt.M + r * mt.cols + c;
-    if (vec && c + 4 <= mt.cols) {
+    if (vec_in && c + 4 <= mt.cols) {
       const float4 v = *reinterpret_cast<const float4*>(src);
       tile[rr][tx * 4 + 0] = v.x;
       tile[rr][tx * 4 + 1] = v.y;
@@ -210,7 +213,7 @@ __global__ void __launch_bounds__(kThreads) normalize_cast_kernel(const RowLaunc
     const int64_t xc = r0 + rr;
     if (xr >= mt.cols) continue;
     __half* dst = mt.X + xr * mt.ldx + xc;
-    if (xc + 4 <= mt.rows) {
+    if (vec_out && xc + 4 <= mt.rows) {
       store_half4(dst, tile[rr][cc] * inv, tile[rr + 1][cc] * inv, tile[rr + 2][cc] * inv, tile[rr + 3][cc] * inv);
     } else {
       for (int k = 0; k < 4; ++k)
