@@ -147,6 +147,32 @@ DMUON_API int dmuon_gemm_f16(int64_t M, int64_t N, int64_t K, const void* A, int
                    float alpha, float beta, float gamma, int symmetric, void* cuda_stream);
 
 /*
+ * dmuon_momentum_normalize_noalloc -- dmuon_momentum_normalize for ONE matrix without any device
+ * allocation. The pages have no counterpart; this exists for callers that cannot allocate device
+ * memory: code whose device memory is owned by someone else (a framework's caching allocator, a fixed
+ * memory plan that must account for every byte) and code that cannot afford the device-wide
+ * synchronisation cudaMalloc / cudaFree may cause. It calls no cudaMalloc, cudaFree or allocating library
+ * routine; its scratch is a fixed array of about 16.5 KB in the library's device image, which every GPU
+ * that loads the library holds until the process exits.
+ *
+ *   grad       device, rows x cols, grad_dtype (fp32 or bf16), or NULL (M is then only read).
+ *   momentum   device fp32 rows x cols; M <- beta * M + G in place.
+ *   x_out      device fp16, min(rows,cols) x max(rows,cols) row-major: X = fp16(M / (||M||_F + eps)),
+ *              transposed when rows > cols.
+ *   norm_out   device fp32, one value: ||M||_F after the update.
+ *   rows*cols must not exceed DMUON_NOALLOC_MAX_ELEMS (2^28); larger matrices are rejected with
+ *   DMUON_ERR_INVALID_ARG before anything is launched.
+ * The first call on a device (with that device current) looks up the scratch's device address; make
+ * that first call before any stream capture. All calls share the one scratch array and it keeps the
+ * last call's contents (nothing in it needs to start at zero), so calls whose work overlaps on the GPU
+ * race with each other: order them on one stream or synchronise between them.
+ */
+#define DMUON_NOALLOC_MAX_ELEMS 268435456
+DMUON_API int dmuon_momentum_normalize_noalloc(const void* grad, int grad_dtype, float* momentum, int64_t rows,
+                                               int64_t cols, void* x_out, float* norm_out, float beta, float eps,
+                                               void* cuda_stream);
+
+/*
  * dmuon_check_status -- synchronise `cuda_stream`, then read and clear the device status word.
  * Returns DMUON_OK, DMUON_ERR_TIMEOUT (a kernel's bounded wait gave up: its results are invalid),
  * DMUON_ERR_NONFINITE (an fp16 intermediate overflowed or was NaN) or DMUON_ERR_CUDA (an

@@ -43,8 +43,9 @@ F32, BF16 = 0, 1
 EXPORTS = (
     "dmuon_ns", "dmuon_muon_step", "dmuon_momentum_normalize", "dmuon_gemm_f16", "dmuon_check_status",
     "dmuon_last_error", "dmuon_version", "dmuon_set_workspace_limit", "dmuon_workspace_size",
-    "dmuon_release_workspace", "dmuon_timing_enable", "dmuon_timing_read",
+    "dmuon_release_workspace", "dmuon_timing_enable", "dmuon_timing_read", "dmuon_momentum_normalize_noalloc",
 )
+NOALLOC_MAX_ELEMS = 268435456
 TIMING_CLASSES = ("momentum_sumsq", "finalize_norms", "normalize_cast", "gemm_tc")
 
 
@@ -85,6 +86,7 @@ def lib():
     L.dmuon_version.restype = ctypes.c_char_p
     L.dmuon_set_workspace_limit.argtypes = [ctypes.c_size_t]
     L.dmuon_workspace_size.argtypes = [i32, _c_i64p, _c_i64p, i32, ctypes.POINTER(ctypes.c_size_t)]
+    L.dmuon_momentum_normalize_noalloc.argtypes = [vp, i32, vp, i64, i64, vp, vp, f32, f32, vp]
     L.dmuon_timing_enable.argtypes = [i32]
     L.dmuon_timing_read.argtypes = [ctypes.POINTER(ctypes.c_double), _c_i64p]
     for name in EXPORTS:
@@ -192,6 +194,15 @@ def momentum_normalize(grads, momenta, x_out, norms_out, beta=0.95, eps=1e-7, st
     cols = (ctypes.c_int64 * n)(*[t.shape[1] for t in momenta])
     _check(lib().dmuon_momentum_normalize(n, G, gd, M, rows, cols, X, _ptr(norms_out), float(beta), float(eps),
                                           _stream(stream)))
+
+
+def momentum_normalize_noalloc(grad, momentum, x_out, norm_out, beta=0.95, eps=1e-7, stream=None):
+    """One matrix of momentum_normalize with no device allocation (fixed library scratch); grad may be
+    None. For callers whose device memory is owned by someone else."""
+    gd = F32 if grad is None else _grad_dtype([grad])
+    _check(lib().dmuon_momentum_normalize_noalloc(_ptr(grad), gd, _ptr(momentum), momentum.shape[0],
+                                                  momentum.shape[1], _ptr(x_out), _ptr(norm_out), float(beta),
+                                                  float(eps), _stream(stream)))
 
 
 def gemm_f16(a, b, d, b_trans=True, e=None, alpha=1.0, beta=0.0, gamma=0.0, symmetric=False, stream=None):

@@ -612,6 +612,9 @@ int check_matrix_list(int count, const int64_t* rows, const int64_t* cols) {
 }
 
 }  // namespace
+
+int set_error(int status, const char* message) { return fail(status, "%s", message); }
+
 }  // namespace dmuon
 
 using namespace dmuon;

@@ -120,4 +120,7 @@ cudaError_t launch_momentum_sumsq(const RowLaunch& p, int64_t nchunks, cudaStrea
 cudaError_t launch_finalize_norms(const RowLaunch& p, cudaStream_t stream);
 cudaError_t launch_normalize_cast(const RowLaunch& p, int64_t ntiles, cudaStream_t stream);
 
+// Record `message` as the calling thread's last error (returned by dmuon_last_error) and return status.
+int set_error(int status, const char* message);
+
 }  // namespace dmuon
