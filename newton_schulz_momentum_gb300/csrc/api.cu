@@ -518,7 +518,8 @@ int bind_plan(DeviceState& ds, Plan& pl, cudaStream_t stream) {
       j.ldd = js.ldd, j.lde = js.lde, j.ldw = js.ldw;
       j.tiles_n = (js.N + bn - 1) / bn;
       const char* err = nullptr;
-      if (!encode_job_maps(j, at(js.a), js.lda, at(js.b), js.ldb, (js.flags & kJobBMnMajor) != 0, bn, &err))
+      if (!encode_job_maps(j, at(js.a), js.lda, at(js.b), js.ldb, (js.flags & kJobBMnMajor) != 0, bn, &err) ||
+          !encode_out_maps(j, &err))
         return fail(DMUON_ERR_CUDA, "%s", err);
       pl.jobs.push_back(j);
     }
@@ -761,7 +762,8 @@ int dmuon_gemm_f16(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, 
     j.ldd = ldd, j.lde = E ? lde : 0;
     j.tiles_n = static_cast<int>((N + bn - 1) / bn);
     const char* err = nullptr;
-    if (!encode_job_maps(j, A, lda, B, ldb, !b_trans, bn, &err)) return fail(DMUON_ERR_CUDA, "%s", err);
+    if (!encode_job_maps(j, A, lda, B, ldb, !b_trans, bn, &err) || !encode_out_maps(j, &err))
+      return fail(DMUON_ERR_CUDA, "%s", err);
     gl.jobs = nullptr;
     gl.tiles = nullptr;
     gl.tiles_m = static_cast<int>((M + kBM - 1) / kBM);

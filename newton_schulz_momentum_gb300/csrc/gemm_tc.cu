@@ -37,8 +37,9 @@ struct Cfg {
   static constexpr int kBBytes = BN * kBK * 2;   // 32 KB or 16 KB
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kTmemCols = 2 * BN;  // two accumulators of BN fp32 columns
+  static constexpr int kEpiBytes = 4 * 4096;  // one 4 KB staging buffer per epilogue warp
   static constexpr int kBarrierBytes = 256;
-  static constexpr int kSmemBytes = kStages * kStageBytes + kBarrierBytes + 1024;  // + alignment slack
+  static constexpr int kSmemBytes = kStages * kStageBytes + kEpiBytes + kBarrierBytes + 1024;  // + alignment slack
   static_assert(kStageBytes % 1024 == 0, "stages must keep 1024-byte alignment for 128B swizzle");
   static_assert((2 * kStages + 5) * 8 + 8 <= kBarrierBytes, "barrier area too small");
 };
@@ -210,6 +211,43 @@ __device__ __forceinline__ TileRef tile_at(const GemmLaunch& p, int t, int bn) {
 }
 
 // ---------------------------------------------------------------------------- epilogue
+//
+// Each epilogue warp owns 32 rows of the tile and walks it in 32-column chunks. A chunk's values are
+// combined in registers, written into the warp's 4 KB staging buffer in shared memory (swizzled so the
+// writes are bank-conflict free) and sent out by one lane with a TMA bulk store: the 32 x 32 fp16 block
+// of D (plus, for symmetric outputs, its transpose at the mirrored position), or, for the final
+// update, the fp32 block reduce-added into W (stored, when W is overwritten). The fp16 addend E of the
+// next chunk is loaded while the current chunk is processed.
+
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t smem_src, int c0, int c1) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1), "r"(smem_src)
+               : "memory");
+}
+
+__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, uint32_t smem_src, int c0, int c1) {
+  asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1), "r"(smem_src)
+               : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// Byte offset of element (r, c) of a 32 x 32 fp16 block: 64-byte rows, 16-byte units swizzled by the
+// TMA 64-byte pattern (unit ^= (r >> 1) & 3). Buffers are 1024-byte aligned.
+__device__ __forceinline__ uint32_t sw64_h(int r, int c) {
+  return static_cast<uint32_t>(r * 64 + ((((c >> 3) ^ (r >> 1)) & 3) << 4) + ((c & 7) << 1));
+}
+// Byte offset of element (r, c) of a 32 x 32 fp32 block: 128-byte rows, 128-byte swizzle (unit ^= r & 7).
+__device__ __forceinline__ uint32_t sw128_f(int r, int c) {
+  return static_cast<uint32_t>(r * 128 + ((((c >> 2) ^ r) & 7) << 4) + ((c & 3) << 2));
+}
 
 struct Scalars {
   float acc, e, diag, d2;
@@ -231,49 +269,59 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
 
 __device__ __forceinline__ bool fp16_ok(float x) { return fabsf(x) < 65520.f; }  // false for NaN too
 
-// Store 32 fp16 values of row i, columns j0.. (all in bounds, 16-byte aligned).
-__device__ __forceinline__ void store_row32(__half* dst, const float (&v)[32]) {
-  uint4* d = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    d[q] = make_uint4(pack_half2(v[8 * q + 0], v[8 * q + 1]), pack_half2(v[8 * q + 2], v[8 * q + 3]),
-                      pack_half2(v[8 * q + 4], v[8 * q + 5]), pack_half2(v[8 * q + 6], v[8 * q + 7]));
-  }
-}
-
 template <int BN>
-__device__ void epilogue_tile(const GemmLaunch& p, const GemmJob& job, int tm, int tn, int quarter,
-                              int lane, uint32_t taddr, bool& bad) {
+__device__ void epilogue_tile(const GemmLaunch& p, const GemmJob& job, int tm, int tn, int quarter, int lane,
+                              uint32_t taddr, uint8_t* stage, bool& bad) {
   const int row0 = tm * kBM + quarter * 32;  // first row handled by this warp
+  if (row0 >= job.M) return;                  // all 32 rows past the edge: nothing to read or store
   const int i = row0 + lane;
   const bool sym = (job.flags & kJobSymmetric) != 0;
   const bool final_out = (job.flags & kJobFinal) != 0;
   const bool final_trans = (job.flags & kJobFinalTrans) != 0;
   const bool has_d2 = (job.flags & kJobD2) != 0;
+  const bool tma_w = final_out && (job.flags & kJobTmaW) && (p.w_alpha == 0.f || p.w_alpha == 1.f);
   const Scalars s = recipe_scalars(p, job.recipe);
-  const bool has_e = job.E != nullptr && s.e != 0.f;
   const bool row_ok = i < job.M;
+  const __half* erow = (job.E != nullptr && s.e != 0.f && row_ok) ? job.E + static_cast<int64_t>(i) * job.lde : nullptr;
+  const bool has_e = job.E != nullptr && s.e != 0.f;
+  const uint32_t sbuf = smem_u32(stage);
 
-  for (int c = 0; c < BN; c += 32) {
+  // Symmetric outputs: chunks left of the diagonal block are produced by the mirrored stores of other
+  // tiles, so this warp starts at its diagonal block (row0 and tn*BN are multiples of 32).
+  int c = sym ? max(0, row0 - tn * BN) : 0;
+  uint4 ecur[4], enext[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) ecur[q] = make_uint4(0, 0, 0, 0), enext[q] = ecur[q];
+  if (erow && c < BN && tn * BN + c + 32 <= job.N) {
+    const uint4* e4 = reinterpret_cast<const uint4*>(erow + tn * BN + c);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) ecur[q] = e4[q];
+  }
+
+  for (; c < BN; c += 32) {
     const int j0 = tn * BN + c;
-    if (j0 >= job.N) break;              // warp-uniform
-    if (sym && j0 < row0) continue;      // whole chunk below the diagonal for every row of this warp
+    if (j0 >= job.N) break;  // warp-uniform
+    const bool full = j0 + 32 <= job.N;
+    const bool prefetch = erow != nullptr && c + 32 < BN && j0 + 64 <= job.N;
+    if (prefetch) {
+      const uint4* e4 = reinterpret_cast<const uint4*>(erow + j0 + 32);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) enext[q] = e4[q];
+    }
     float v[32];
     tmem_ld32(taddr + static_cast<uint32_t>(c), v);
-    if (!row_ok) continue;
-    const bool full = j0 + 32 <= job.N;
 
-    if (has_e) {
-      const __half* erow = job.E + static_cast<int64_t>(i) * job.lde + j0;
+    if (!row_ok) {
+#pragma unroll
+      for (int k = 0; k < 32; ++k) v[k] = 0.f;
+    } else if (has_e) {
       if (full) {
-        const uint4* e4 = reinterpret_cast<const uint4*>(erow);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          uint4 u = e4[q];
-          const __half2* h = reinterpret_cast<const __half2*>(&u);
+          const __half2* h = reinterpret_cast<const __half2*>(&ecur[q]);
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
-            float2 f = __half22float2(h[k]);
+            const float2 f = __half22float2(h[k]);
             v[8 * q + 2 * k] = fmaf(s.acc, v[8 * q + 2 * k], s.e * f.x);
             v[8 * q + 2 * k + 1] = fmaf(s.acc, v[8 * q + 2 * k + 1], s.e * f.y);
           }
@@ -281,7 +329,7 @@ __device__ void epilogue_tile(const GemmLaunch& p, const GemmJob& job, int tm, i
       } else {
 #pragma unroll
         for (int k = 0; k < 32; ++k) {
-          const float e = (j0 + k < job.N) ? __half2float(erow[k]) : 0.f;
+          const float e = (j0 + k < job.N) ? __half2float(erow[j0 + k]) : 0.f;
           v[k] = fmaf(s.acc, v[k], s.e * e);
         }
       }
@@ -294,43 +342,49 @@ __device__ void epilogue_tile(const GemmLaunch& p, const GemmJob& job, int tm, i
       for (int k = 0; k < 32; ++k)
         if (j0 + k == i) v[k] += s.diag;
     }
+    if (prefetch) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) ecur[q] = enext[q];
+    }
 
     if (final_out) {
-      // W = w_alpha * W + w_beta * v, W in the caller's orientation.
-      if (!final_trans) {
-        float* wrow = job.W + static_cast<int64_t>(i) * job.ldw + j0;
-        const bool vec = full && ((job.ldw & 3) == 0) && ((reinterpret_cast<uintptr_t>(job.W) & 15) == 0);
-        if (vec) {
-          float4* w4 = reinterpret_cast<float4*>(wrow);
 #pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            float4 w = p.w_alpha != 0.f ? w4[q] : make_float4(0.f, 0.f, 0.f, 0.f);
-            w.x = p.w_alpha * w.x + p.w_beta * v[4 * q + 0];
-            w.y = p.w_alpha * w.y + p.w_beta * v[4 * q + 1];
-            w.z = p.w_alpha * w.z + p.w_beta * v[4 * q + 2];
-            w.w = p.w_alpha * w.w + p.w_beta * v[4 * q + 3];
-            bad |= !(isfinite(w.x) && isfinite(w.y) && isfinite(w.z) && isfinite(w.w));
-            w4[q] = w;
-          }
+      for (int k = 0; k < 32; ++k) bad |= (j0 + k < job.N) && !isfinite(v[k]);
+      if (tma_w) {
+        if (lane == 0) bulk_wait_read0();
+        __syncwarp();
+        if (!final_trans) {
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            *reinterpret_cast<float4*>(stage + sw128_f(lane, 4 * q)) =
+                make_float4(p.w_beta * v[4 * q], p.w_beta * v[4 * q + 1], p.w_beta * v[4 * q + 2], p.w_beta * v[4 * q + 3]);
+        } else {
+#pragma unroll
+          for (int k = 0; k < 32; ++k) *reinterpret_cast<float*>(stage + sw128_f(k, lane)) = p.w_beta * v[k];
+        }
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          const int x = final_trans ? row0 : j0;
+          const int y = final_trans ? j0 : row0;
+          if (p.w_alpha == 0.f) tma_store_2d(&job.tmW, sbuf, x, y);
+          else tma_reduce_add_2d(&job.tmW, sbuf, x, y);
+          bulk_commit();
+        }
+      } else if (row_ok) {
+        // W rows not 16-byte aligned: direct read-modify-write.
+        if (!final_trans) {
+          float* wrow = job.W + static_cast<int64_t>(i) * job.ldw + j0;
+#pragma unroll
+          for (int k = 0; k < 32; ++k)
+            if (j0 + k < job.N) wrow[k] = (p.w_alpha != 0.f ? p.w_alpha * wrow[k] : 0.f) + p.w_beta * v[k];
         } else {
 #pragma unroll
           for (int k = 0; k < 32; ++k) {
             if (j0 + k < job.N) {
-              const float w = (p.w_alpha != 0.f ? p.w_alpha * wrow[k] : 0.f) + p.w_beta * v[k];
-              bad |= !isfinite(w);
-              wrow[k] = w;
+              float* w = job.W + static_cast<int64_t>(j0 + k) * job.ldw + i;
+              *w = (p.w_alpha != 0.f ? p.w_alpha * *w : 0.f) + p.w_beta * v[k];
             }
-          }
-        }
-      } else {
-        // Kernel row i is the caller's column i: consecutive lanes write consecutive addresses.
-#pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          if (j0 + k < job.N) {
-            float* w = job.W + static_cast<int64_t>(j0 + k) * job.ldw + i;
-            const float nw = (p.w_alpha != 0.f ? p.w_alpha * *w : 0.f) + p.w_beta * v[k];
-            bad |= !isfinite(nw);
-            *w = nw;
           }
         }
       }
@@ -338,46 +392,55 @@ __device__ void epilogue_tile(const GemmLaunch& p, const GemmJob& job, int tm, i
     }
 
 #pragma unroll
-    for (int k = 0; k < 32; ++k) bad |= !fp16_ok(v[k]);
+    for (int k = 0; k < 32; ++k) bad |= (j0 + k < job.N) && !fp16_ok(v[k]);
+    const bool upper = sym && j0 > row0;  // strictly above the diagonal for every row of the block
+    const bool on_diag = j0 == row0;      // the block holds the diagonal elements i == j
 
-    // Symmetric outputs: chunks with j0 > row0 lie strictly above the diagonal for every row here.
-    const bool upper_chunk = sym && j0 > row0;
-    const bool diag_chunk = sym && j0 == row0;
-    for (int pass = 0; pass < (has_d2 ? 2 : 1); ++pass) {
-      __half* out = pass == 0 ? job.D : job.D2;
-      if (pass == 1) {
+    if (lane == 0) bulk_wait_read0();  // the previous chunk's stores have read the buffer
+    __syncwarp();
 #pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          if (j0 + k == i) {
-            v[k] += s.d2;
-            bad |= !fp16_ok(v[k]);
-          }
-        }
+    for (int q = 0; q < 4; ++q)
+      *reinterpret_cast<uint4*>(stage + sw64_h(lane, 8 * q)) =
+          make_uint4(pack_half2(v[8 * q + 0], v[8 * q + 1]), pack_half2(v[8 * q + 2], v[8 * q + 3]),
+                     pack_half2(v[8 * q + 4], v[8 * q + 5]), pack_half2(v[8 * q + 6], v[8 * q + 7]));
+    if (upper) {
+#pragma unroll
+      for (int k = 0; k < 32; ++k) *reinterpret_cast<__half*>(stage + 2048 + sw64_h(k, lane)) = __float2half_rn(v[k]);
+    }
+    __syncwarp();
+    if (sym && on_diag) {
+      // Lower triangle of the diagonal block takes the upper-triangle values (exact symmetry).
+#pragma unroll
+      for (int k = 0; k < 32; ++k)
+        if (k < lane) *reinterpret_cast<__half*>(stage + sw64_h(lane, k)) = *reinterpret_cast<const __half*>(stage + sw64_h(k, lane));
+      __syncwarp();
+    }
+    fence_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_2d(&job.tmD, sbuf, j0, row0);
+      if (upper) tma_store_2d(&job.tmD, sbuf + 2048, row0, j0);
+      if (has_d2 && !on_diag) {
+        tma_store_2d(&job.tmD2, sbuf, j0, row0);
+        if (upper) tma_store_2d(&job.tmD2, sbuf + 2048, row0, j0);
       }
-      __half* orow = out + static_cast<int64_t>(i) * job.ldd + j0;
-      if (!sym || upper_chunk) {
-        if (full) {
-          store_row32(orow, v);
-        } else {
+      bulk_commit();
+    }
+    if (has_d2 && on_diag) {
+      // D2 = D + a I: only the diagonal elements of this block differ.
+      float dv = 0.f;
 #pragma unroll
-          for (int k = 0; k < 32; ++k)
-            if (j0 + k < job.N) orow[k] = __float2half_rn(v[k]);
-        }
-        if (upper_chunk) {
-#pragma unroll
-          for (int k = 0; k < 32; ++k)
-            if (j0 + k < job.N) out[static_cast<int64_t>(j0 + k) * job.ldd + i] = __float2half_rn(v[k]);
-        }
-      } else if (diag_chunk) {
-#pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          const int j = j0 + k;
-          if (j < job.N && j >= i) {
-            const __half h = __float2half_rn(v[k]);
-            orow[k] = h;
-            if (j > i) out[static_cast<int64_t>(j) * job.ldd + i] = h;
-          }
-        }
+      for (int k = 0; k < 32; ++k)
+        if (k == lane) dv = v[k] + s.d2;
+      bad |= row_ok && !fp16_ok(dv);
+      if (lane == 0) bulk_wait_read0();
+      __syncwarp();
+      *reinterpret_cast<__half*>(stage + sw64_h(lane, lane)) = __float2half_rn(dv);
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_2d(&job.tmD2, sbuf, j0, row0);
+        bulk_commit();
       }
     }
   }
@@ -390,7 +453,8 @@ __global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__
   using C = Cfg<BN>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStageBytes);
+  uint8_t* epi_stage = smem + C::kStages * C::kStageBytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(epi_stage + C::kEpiBytes);
   uint64_t* empty = full + C::kStages;
   uint64_t* tfull = empty + C::kStages;
   uint64_t* tempty = tfull + 2;
@@ -532,13 +596,14 @@ __global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__
       tc_fence_after();
       const uint32_t taddr =
           tmem_base + static_cast<uint32_t>(acc * BN) + (static_cast<uint32_t>(quarter * 32) << 16);
-      epilogue_tile<BN>(p, *tr.job, tr.tm, tr.tn, quarter, lane, taddr, bad);
+      epilogue_tile<BN>(p, *tr.job, tr.tm, tr.tn, quarter, lane, taddr, epi_stage + (warp - 2) * 4096, bad);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty[acc]);
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
+    if (lane == 0) bulk_wait0();  // every bulk store / reduce of this warp has completed
     if (bad) atomicOr(p.status, kDevNonfinite);
   }
 
@@ -571,9 +636,11 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 2-D fp16 map: `inner` contiguous elements per row, `outer` rows `row_bytes` apart.
+// 2-D map: `inner` contiguous elements per row, `outer` rows `row_bytes` apart.
 bool encode_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
-               uint32_t box_inner, uint32_t box_outer, const char** err) {
+               uint32_t box_inner, uint32_t box_outer, const char** err,
+               CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+               CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) {
     *err = "cuTensorMapEncodeTiled is not available from the CUDA driver";
@@ -583,9 +650,9 @@ bool encode_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t oute
   const cuuint64_t strides[1] = {row_bytes};
   const cuuint32_t box[2] = {box_inner, box_outer};
   const cuuint32_t estr[2] = {1, 1};
-  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-                        estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  const CUresult r = fn(map, dtype, 2, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     *err = "cuTensorMapEncodeTiled rejected an operand (alignment, stride or size)";
     return false;
@@ -607,6 +674,29 @@ bool encode_job_maps(GemmJob& job, const void* a, int64_t lda, const void* b, in
                      static_cast<uint64_t>(ldb) * 2, kBK, static_cast<uint32_t>(bn), err);
   return encode_2d(&job.tmB, b, static_cast<uint64_t>(job.N), static_cast<uint64_t>(job.K),
                    static_cast<uint64_t>(ldb) * 2, 64, kBK, err);
+}
+
+bool encode_out_maps(GemmJob& job, const char** err) {
+  if (job.D && !encode_2d(&job.tmD, job.D, static_cast<uint64_t>(job.N), static_cast<uint64_t>(job.M),
+                          static_cast<uint64_t>(job.ldd) * 2, 32, 32, err, CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                          CU_TENSOR_MAP_SWIZZLE_64B))
+    return false;
+  if (job.D2 && !encode_2d(&job.tmD2, job.D2, static_cast<uint64_t>(job.N), static_cast<uint64_t>(job.M),
+                           static_cast<uint64_t>(job.ldd) * 2, 32, 32, err, CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                           CU_TENSOR_MAP_SWIZZLE_64B))
+    return false;
+  job.flags &= ~kJobTmaW;
+  if ((job.flags & kJobFinal) && job.W && (reinterpret_cast<uintptr_t>(job.W) & 15) == 0 && (job.ldw & 3) == 0) {
+    // W in the caller's orientation: M x N, or N x M when the matrix was worked on transposed.
+    const bool tr = (job.flags & kJobFinalTrans) != 0;
+    const uint64_t inner = static_cast<uint64_t>(tr ? job.M : job.N);
+    const uint64_t outer = static_cast<uint64_t>(tr ? job.N : job.M);
+    const char* e2 = nullptr;
+    if (encode_2d(&job.tmW, job.W, inner, outer, static_cast<uint64_t>(job.ldw) * 4, 32, 32, &e2,
+                  CU_TENSOR_MAP_DATA_TYPE_FLOAT32, CU_TENSOR_MAP_SWIZZLE_128B))
+      job.flags |= kJobTmaW;
+  }
+  return true;
 }
 
 cudaError_t launch_gemm(const GemmLaunch& p, int bn, int grid, cudaStream_t stream) {

@@ -41,11 +41,15 @@ enum JobFlags : int {
   kJobFinal = 4,       // write fp32 W = w_alpha * W + w_beta * v instead of an fp16 D
   kJobFinalTrans = 8,  // with kJobFinal: W is stored transposed (W[j][i])
   kJobD2 = 16,         // also store D2 = v + a * [i == j] (the first Q after a (re)start)
+  kJobTmaW = 32,       // with kJobFinal: tmW is valid (W rows 16-byte aligned) -> TMA store / reduce-add
 };
 
 struct alignas(128) GemmJob {
-  CUtensorMap tmA;  // A: M rows x K cols (K contiguous), box {64, 128}
-  CUtensorMap tmB;  // B: N x K (K contiguous) box {64, BN}, or K x N (N contiguous) box {64, 64}
+  CUtensorMap tmA;   // A: M rows x K cols (K contiguous), box {64, 128}
+  CUtensorMap tmB;   // B: N x K (K contiguous) box {64, BN}, or K x N (N contiguous) box {64, 64}
+  CUtensorMap tmD;   // D (fp16, M x N, ldd), box {32, 32}, 64-byte swizzle: epilogue TMA stores
+  CUtensorMap tmD2;  // D2, same geometry
+  CUtensorMap tmW;   // W (fp32, caller orientation), box {32, 32}, 128-byte swizzle (kJobTmaW)
   __half* D;
   __half* D2;
   const __half* E;
@@ -83,6 +87,10 @@ int gemm_smem_bytes(int bn);
 // b_mn_major selects the K x N storage of Bop. Returns false (with a message) on failure.
 bool encode_job_maps(GemmJob& job, const void* a, int64_t lda, const void* b, int64_t ldb,
                      bool b_mn_major, int bn, const char** err);
+// Encode the epilogue maps of a job from its D, D2, W pointers and leading dimensions (host). Sets
+// kJobTmaW when the W map can be built (16-byte aligned base and rows); otherwise the final update
+// falls back to direct stores.
+bool encode_out_maps(GemmJob& job, const char** err);
 
 // ------------------------------------------------------------------------------------------------
 // Row-wise (HBM-bound) kernels (rowwise.cu): momentum + sum of squares, norm finalisation,
