@@ -196,11 +196,27 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def max_over_ranks(ms, device):
+    """Largest per-rank time (ms) across the process group; the job is as slow as its slowest rank."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(ms)
+    t = torch.tensor([float(ms)], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(flops_per_rank_step, world, ms_per_step):
+    """Weak scaling: every rank updates its own full matrix set, so the job does world x the work."""
+    return world * flops_per_rank_step / (ms_per_step * 1e-3) / 1e12
+
+
 def run_e2e(args, G, norms, step, barrier, stream, world, flops_step):
     """Same metric through the public call, with each step's gradients copied in from pinned host memory
     and the per-matrix norms (the step's reported result) read back, all inside the timed region."""
     import torch
-    import torch.distributed as dist
 
     host_g = [g.cpu().pin_memory() for g in G]
     host_norms = torch.empty(norms.numel(), dtype=torch.float32).pin_memory()
@@ -216,13 +232,9 @@ def run_e2e(args, G, norms, step, barrier, stream, world, flops_step):
         host_norms.copy_(norms, non_blocking=True)
     stop.record(stream)
     barrier()
-    ms = start.elapsed_time(stop)
-    if world > 1:
-        t = torch.tensor([ms], device=norms.device, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(start.elapsed_time(stop), norms.device)
     del host_g
-    return {"value": world * flops_step / (ms / args.e2e_steps * 1e-3) / 1e12, "unit": UNIT,
+    return {"value": whole_job_tflops(flops_step, world, ms / args.e2e_steps), "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms / args.e2e_steps}
 
 
@@ -280,16 +292,11 @@ def run_native(args):
             step()
         stop.record(stream)
         barrier()
-    ms = start.elapsed_time(stop)
     kernel_times = dm.timing_read()
     dm.timing_enable(False)
     dm.check_status(stream)
-    if world > 1:
-        t = torch.tensor([ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    ms_step = ms / args.steps
-    value = world * flops_step / (ms_step * 1e-3) / 1e12
+    ms_step = max_over_ranks(start.elapsed_time(stop), dev) / args.steps
+    value = whole_job_tflops(flops_step, world, ms_step)
 
     # ---- end to end through the public call: pinned host gradients in, norms out
     e2e = None
