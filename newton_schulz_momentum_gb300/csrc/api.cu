@@ -16,6 +16,7 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <string>
@@ -91,7 +92,7 @@ struct JobSpec {
 };
 
 struct LaunchRec {
-  int first_job, njobs, first_tile, ntiles, bn, coef;
+  int first_job, njobs, first_tile, ntiles, tile, coef;
 };
 
 struct Plan {
@@ -361,10 +362,19 @@ void build_direct_phases(Plan& pl, int steps) {
   }
 }
 
-int launch_bn(const std::vector<JobSpec>& ph) {
-  for (const JobSpec& j : ph)
-    if (j.N > 128) return 256;
-  return 128;
+// Tile configuration of a launch: 128 x 128 single-CTA tiles when every product is at most 128 wide,
+// otherwise 256 x 256 tiles on CTA pairs (DMUON_GEMM_TILE=single selects 128 x 256 single-CTA tiles).
+int pick_tile(int max_n) {
+  if (max_n <= 128) return kTileSingle128;
+  const char* env = getenv("DMUON_GEMM_TILE");
+  if (env && strcmp(env, "single") == 0) return kTileSingle256;
+  return kTilePair256;
+}
+
+int launch_tile(const std::vector<JobSpec>& ph) {
+  int max_n = 0;
+  for (const JobSpec& j : ph) max_n = std::max(max_n, j.N);
+  return pick_tile(max_n);
 }
 
 // Host-side plan: matrix layout, workspace offsets, phases, tiles. No device calls.
@@ -454,16 +464,17 @@ int build_plan_host(Plan& pl, const PlanKey& key, const std::vector<const void*>
     LaunchRec L;
     L.first_job = 0;  // filled below
     L.njobs = static_cast<int>(ph.size());
-    L.bn = launch_bn(ph);
+    L.tile = launch_tile(ph);
     L.coef = pl.phase_coef[p];
     L.first_tile = static_cast<int>(pl.tiles.size());
+    const int th = tile_rows(L.tile), tw = tile_cols(L.tile);
     for (int j = 0; j < L.njobs; ++j) {
       const JobSpec& js = ph[j];
-      const int tm_n = (js.M + kBM - 1) / kBM;
-      const int tn_n = (js.N + L.bn - 1) / L.bn;
+      const int tm_n = (js.M + th - 1) / th;
+      const int tn_n = (js.N + tw - 1) / tw;
       for (int tm = 0; tm < tm_n; ++tm)
         for (int tn = 0; tn < tn_n; ++tn) {
-          if ((js.flags & kJobSymmetric) && tn * L.bn + L.bn - 1 < tm * kBM) continue;
+          if ((js.flags & kJobSymmetric) && tn * tw + tw - 1 < tm * th) continue;
           pl.tiles.push_back(GemmTile{j, tm, tn, 0});
         }
     }
@@ -505,7 +516,7 @@ int bind_plan(DeviceState& ds, Plan& pl, cudaStream_t stream) {
   }
   pl.jobs.clear();
   for (size_t p = 0; p < pl.phases.size(); ++p) {
-    const int bn = pl.launches[p].bn;
+    const int tile = pl.launches[p].tile;
     for (const JobSpec& js : pl.phases[p]) {
       GemmJob j;
       std::memset(&j, 0, sizeof(j));
@@ -516,9 +527,9 @@ int bind_plan(DeviceState& ds, Plan& pl, cudaStream_t stream) {
       j.E = static_cast<const __half*>(at(js.e));
       j.W = js.W;
       j.ldd = js.ldd, j.lde = js.lde, j.ldw = js.ldw;
-      j.tiles_n = (js.N + bn - 1) / bn;
+      j.tiles_n = (js.N + tile_cols(tile) - 1) / tile_cols(tile);
       const char* err = nullptr;
-      if (!encode_job_maps(j, at(js.a), js.lda, at(js.b), js.ldb, (js.flags & kJobBMnMajor) != 0, bn, &err) ||
+      if (!encode_job_maps(j, at(js.a), js.lda, at(js.b), js.ldb, (js.flags & kJobBMnMajor) != 0, tile, &err) ||
           !encode_out_maps(j, &err))
         return fail(DMUON_ERR_CUDA, "%s", err);
       pl.jobs.push_back(j);
@@ -572,8 +583,8 @@ int run_plan(DeviceState& ds, const Plan& pl, const float* coeffs, float lr, flo
     gl.w_alpha = pl.key.kind == kPlanNs ? 0.f : 1.f;
     gl.w_beta = pl.key.kind == kPlanNs ? 1.f : -lr;
     gl.status = ds.status;
-    const int grid = std::min(L.ntiles, ds.sms);
-    DM_CUDA(timed(3, stream, [&] { return launch_gemm(gl, L.bn, grid, stream); }), "tensor-core GEMM launch");
+    const int units = std::min(L.ntiles, gemm_max_units(L.tile, ds.sms));
+    DM_CUDA(timed(3, stream, [&] { return launch_gemm(gl, L.tile, units, stream); }), "tensor-core GEMM launch");
   }
   return DMUON_OK;
 }
@@ -750,7 +761,7 @@ int dmuon_gemm_f16(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, 
     DeviceState* ds = nullptr;
     int st = current_device(&ds);
     if (st != DMUON_OK) return st;
-    const int bn = N > 128 ? 256 : 128;
+    const int tile = pick_tile(static_cast<int>(N));
     GemmLaunch gl;
     std::memset(&gl, 0, sizeof(gl));
     GemmJob& j = gl.single;
@@ -760,21 +771,21 @@ int dmuon_gemm_f16(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, 
     j.D = static_cast<__half*>(D);
     j.E = static_cast<const __half*>(E);
     j.ldd = ldd, j.lde = E ? lde : 0;
-    j.tiles_n = static_cast<int>((N + bn - 1) / bn);
+    j.tiles_n = static_cast<int>((N + tile_cols(tile) - 1) / tile_cols(tile));
     const char* err = nullptr;
-    if (!encode_job_maps(j, A, lda, B, ldb, !b_trans, bn, &err) || !encode_out_maps(j, &err))
+    if (!encode_job_maps(j, A, lda, B, ldb, !b_trans, tile, &err) || !encode_out_maps(j, &err))
       return fail(DMUON_ERR_CUDA, "%s", err);
     gl.jobs = nullptr;
     gl.tiles = nullptr;
-    gl.tiles_m = static_cast<int>((M + kBM - 1) / kBM);
+    gl.tiles_m = static_cast<int>((M + tile_rows(tile) - 1) / tile_rows(tile));
     const int64_t ntiles = static_cast<int64_t>(gl.tiles_m) * j.tiles_n;
     if (ntiles >= (int64_t(1) << 31)) return fail(DMUON_ERR_UNSUPPORTED, "too many tiles");
     gl.ntiles = static_cast<int>(ntiles);
     gl.alpha = alpha, gl.beta = E ? beta : 0.f, gl.gamma = gamma;
     gl.status = ds->status;
-    const int grid = static_cast<int>(std::min<int64_t>(ntiles, ds->sms));
+    const int units = static_cast<int>(std::min<int64_t>(ntiles, gemm_max_units(tile, ds->sms)));
     cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
-    DM_CUDA(timed(3, stream, [&] { return launch_gemm(gl, bn, grid, stream); }), "tensor-core GEMM launch");
+    DM_CUDA(timed(3, stream, [&] { return launch_gemm(gl, tile, units, stream); }), "tensor-core GEMM launch");
     return DMUON_OK;
   } catch (const std::exception& e) {
     return fail(DMUON_ERR_OOM, "host exception: %s", e.what());

@@ -20,6 +20,7 @@
 // Every mbarrier wait is bounded: after kWaitLimitNs the waiting thread raises a CTA-wide abort
 // flag and sets kDevTimeout in the device status word, all roles leave their loops, in-flight copies
 // and MMAs are drained (again with a bound), tensor memory is freed and the kernel returns.
+#include <algorithm>
 #include <cstdio>
 
 #include "internal.h"
@@ -30,18 +31,23 @@ namespace {
 constexpr unsigned long long kWaitLimitNs = 4000000000ull;  // 4 s: far above any legitimate wait
 constexpr unsigned long long kDrainLimitNs = 200000000ull;  // 0.2 s for draining after an abort
 
-template <int BN>
+// BN: output tile width. CG: CTAs per MMA (1, or 2 for a CTA pair sharing one 256 x BN tile with
+// tcgen05.mma.cta_group::2; each CTA then holds 128 rows of A and BN / 2 rows of B per stage).
+template <int BN, int CG>
 struct Cfg {
-  static constexpr int kStages = (BN == 256) ? 4 : 6;
+  static constexpr int kBRows = BN / CG;         // rows of the B tile held by one CTA
+  static constexpr int kTileM = kBM * CG;        // output rows per tile
   static constexpr int kABytes = kBM * kBK * 2;  // 16 KB
-  static constexpr int kBBytes = BN * kBK * 2;   // 32 KB or 16 KB
+  static constexpr int kBBytes = kBRows * kBK * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kStages = (kStageBytes <= 32768) ? 6 : 4;
   static constexpr int kTmemCols = 2 * BN;  // two accumulators of BN fp32 columns
   static constexpr int kEpiBytes = 4 * 4096;  // one 4 KB staging buffer per epilogue warp
   static constexpr int kBarrierBytes = 256;
   static constexpr int kSmemBytes = kStages * kStageBytes + kEpiBytes + kBarrierBytes + 1024;  // + alignment slack
   static_assert(kStageBytes % 1024 == 0, "stages must keep 1024-byte alignment for 128B swizzle");
   static_assert((2 * kStages + 5) * 8 + 8 <= kBarrierBytes, "barrier area too small");
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
 // ---------------------------------------------------------------------------- PTX wrappers
@@ -117,6 +123,38 @@ __device__ __forceinline__ void tma_load_2d(uint32_t smem_dst, const CUtensorMap
       : "memory");
 }
 
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// shared::cluster address of this CTA's shared variable at `addr` as seen in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_shared(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+
+// CTA-pair load: the data lands in this CTA's shared memory, completion is signalled on the mbarrier at
+// shared::cluster address `mbar` (the pair's leader).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t smem_dst, const CUtensorMap* map, int c0, int c1,
+                                                 uint32_t mbar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(mbar)
+      : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t mbar_cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(mbar_cluster_addr) : "memory");
+}
+
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
@@ -134,10 +172,10 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
 
 // Instruction descriptor for kind::f16: fp32 accumulator (bit 4), A and B fp16 (format 0), A K-major,
 // B K-major or MN-major (bit 16), N >> 3 at bits 17-22, M >> 4 at bits 24-28.
-template <int BN>
+template <int BM, int BN>
 __device__ __forceinline__ uint32_t instr_desc(bool b_mn_major) {
   return (1u << 4) | ((b_mn_major ? 1u : 0u) << 16) | (static_cast<uint32_t>(BN >> 3) << 17) |
-         (static_cast<uint32_t>(kBM >> 4) << 24);
+         (static_cast<uint32_t>(BM >> 4) << 24);
 }
 
 __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
@@ -148,6 +186,32 @@ __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
+}
+
+__device__ __forceinline__ void mma_f16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                             uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive on the mbarrier at this shared offset in both CTAs of the pair once this thread's MMAs finish.
+__device__ __forceinline__ void mma_commit_pair(uint64_t* bar) {
+  const uint16_t mask = 3;
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          smem_u32(bar)),
+      "h"(mask)
+      : "memory");
+}
+
+// Completion of this thread's CTA-pair MMAs, signalled on this CTA's barrier only.
+__device__ __forceinline__ void mma_commit_pair_local(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
 }
 
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
@@ -165,6 +229,19 @@ __device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
 
 __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
   asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// CTA-pair allocation: executed by one warp in each CTA of the pair; the same columns are allocated in
+// both CTAs' tensor memory.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t* slot, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot)),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
 
 // 32 consecutive fp32 columns of this thread's TMEM lane.
@@ -193,7 +270,7 @@ struct TileRef {
   bool skip;  // a lower-triangle tile of a symmetric single-job launch: nobody touches it
 };
 
-__device__ __forceinline__ TileRef tile_at(const GemmLaunch& p, int t, int bn) {
+__device__ __forceinline__ TileRef tile_at(const GemmLaunch& p, int t, int bn, int tile_m) {
   TileRef r;
   if (p.jobs != nullptr) {
     const GemmTile g = p.tiles[t];
@@ -205,7 +282,7 @@ __device__ __forceinline__ TileRef tile_at(const GemmLaunch& p, int t, int bn) {
     r.job = &p.single;
     r.tm = t / p.single.tiles_n;
     r.tn = t - r.tm * p.single.tiles_n;
-    r.skip = (p.single.flags & kJobSymmetric) && (r.tn * bn + bn - 1 < r.tm * kBM);
+    r.skip = (p.single.flags & kJobSymmetric) && (r.tn * bn + bn - 1 < r.tm * tile_m);
   }
   return r;
 }
@@ -270,9 +347,9 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
 __device__ __forceinline__ bool fp16_ok(float x) { return fabsf(x) < 65520.f; }  // false for NaN too
 
 template <int BN>
-__device__ void epilogue_tile(const GemmLaunch& p, const GemmJob& job, int tm, int tn, int quarter, int lane,
-                              uint32_t taddr, uint8_t* stage, bool& bad) {
-  const int row0 = tm * kBM + quarter * 32;  // first row handled by this warp
+__device__ void epilogue_tile(const GemmLaunch& p, const GemmJob& job, int tile_row0, int tn, int quarter,
+                              int lane, uint32_t taddr, uint8_t* stage, bool& bad) {
+  const int row0 = tile_row0 + quarter * 32;  // first row handled by this warp
   if (row0 >= job.M) return;                  // all 32 rows past the edge: nothing to read or store
   const int i = row0 + lane;
   const bool sym = (job.flags & kJobSymmetric) != 0;
@@ -448,9 +525,10 @@ __device__ void epilogue_tile(const GemmLaunch& p, const GemmJob& job, int tm, i
 
 // ---------------------------------------------------------------------------- the kernel
 
-template <int BN>
-__global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__ GemmLaunch p) {
-  using C = Cfg<BN>;
+template <int BN, int CG>
+__device__ __forceinline__ void gemm_tc_body(const GemmLaunch& p) {
+  using C = Cfg<BN, CG>;
+  constexpr bool kPair = CG == 2;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* epi_stage = smem + C::kStages * C::kStageBytes;
@@ -464,6 +542,9 @@ __global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const uint32_t rank = kPair ? cluster_ctarank() : 0u;  // 0 = the pair's leader (issues the MMAs)
+  const int unit = kPair ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int nunits = kPair ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
@@ -472,15 +553,19 @@ __global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 4);
+      mbar_init(&tempty[a], 4 * CG);  // every epilogue warp of the pair releases the accumulator
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == 1) tmem_alloc(tmem_slot, C::kTmemCols);
+  if (warp == 1) {
+    if constexpr (kPair) tmem_alloc_pair(tmem_slot, C::kTmemCols);
+    else tmem_alloc(tmem_slot, C::kTmemCols);
+  }
   tc_fence_before();
   __syncthreads();
+  if constexpr (kPair) cluster_sync_all();  // the peer's barriers are initialised before anyone signals them
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -494,14 +579,14 @@ __global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__
 #pragma unroll
       for (int s = 0; s < C::kStages; ++s) issued[s] = 0, issued_parity[s] = 0;
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < p.ntiles; t += gridDim.x) {
-        const TileRef tr = tile_at(p, t, BN);
+      for (int t = unit; ok && t < p.ntiles; t += nunits) {
+        const TileRef tr = tile_at(p, t, BN, C::kTileM);
         if (tr.skip) continue;
         const GemmJob* job = tr.job;
         const int nkb = (job->K + kBK - 1) / kBK;
         const bool bmn = (job->flags & kJobBMnMajor) != 0;
-        const int m0 = tr.tm * kBM;
-        const int n0 = tr.tn * BN;
+        const int m0 = tr.tm * C::kTileM + static_cast<int>(rank) * kBM;   // this CTA's 128 rows of A
+        const int n0 = tr.tn * BN + static_cast<int>(rank) * C::kBRows;   // this CTA's rows of B
         for (int kb = 0; kb < nkb; ++kb) {
           if (!wait_bounded(&empty[stage], phase ^ 1u, abort_flag, p.status, kWaitLimitNs, true)) {
             ok = false;
@@ -509,13 +594,27 @@ __global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__
           }
           const uint32_t sa = smem_u32(smem + stage * C::kStageBytes);
           const uint32_t sb = sa + C::kABytes;
-          mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
-          tma_load_2d(sa, &job->tmA, kb * kBK, m0, &full[stage]);
-          if (!bmn) {
-            tma_load_2d(sb, &job->tmB, kb * kBK, n0, &full[stage]);
-          } else {
+          if constexpr (kPair) {
+            // Both CTAs' copies complete on the leader's full barrier; the leader expects both.
+            const uint32_t bar = map_shared(smem_u32(&full[stage]), 0);
+            if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * C::kStageBytes);
+            tma_load_2d_pair(sa, &job->tmA, kb * kBK, m0, bar);
+            if (!bmn) {
+              tma_load_2d_pair(sb, &job->tmB, kb * kBK, n0, bar);
+            } else {
 #pragma unroll
-            for (int q = 0; q < BN / 64; ++q) tma_load_2d(sb + q * 8192, &job->tmB, n0 + q * 64, kb * kBK, &full[stage]);
+              for (int q = 0; q < C::kBRows / 64; ++q)
+                tma_load_2d_pair(sb + q * 8192, &job->tmB, n0 + q * 64, kb * kBK, bar);
+            }
+          } else {
+            mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
+            tma_load_2d(sa, &job->tmA, kb * kBK, m0, &full[stage]);
+            if (!bmn) {
+              tma_load_2d(sb, &job->tmB, kb * kBK, n0, &full[stage]);
+            } else {
+#pragma unroll
+              for (int q = 0; q < C::kBRows / 64; ++q) tma_load_2d(sb + q * 8192, &job->tmB, n0 + q * 64, kb * kBK, &full[stage]);
+            }
           }
           issued[stage] = 1;
           issued_parity[stage] = phase;
@@ -525,22 +624,24 @@ __global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__
           }
         }
       }
-      if (!ok) {
+      if (!ok && !kPair) {
         // Aborting: let every copy already issued land before the CTA's shared memory is released.
         for (int s = 0; s < C::kStages; ++s)
           if (issued[s]) wait_bounded(&full[s], issued_parity[s], abort_flag, p.status, kDrainLimitNs, false);
       }
+      // (A pair's copies complete on the leader's barriers; the closing cluster barrier plus the
+      // leader's drain keep both CTAs resident until then.)
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // ------------------------------------------------------------------ MMA issuer (the leader only)
+    if (lane == 0 && rank == 0) {
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < p.ntiles; t += gridDim.x) {
-        const TileRef tr = tile_at(p, t, BN);
+      for (int t = unit; ok && t < p.ntiles; t += nunits) {
+        const TileRef tr = tile_at(p, t, BN, C::kTileM);
         if (tr.skip) continue;
         const GemmJob* job = tr.job;
         const int nkb = (job->K + kBK - 1) / kBK;
@@ -548,7 +649,7 @@ __global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__
         if (!wait_bounded(&tempty[acc], acc_phase ^ 1u, abort_flag, p.status, kWaitLimitNs, true)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-        const uint32_t idesc = instr_desc<BN>(bmn);
+        const uint32_t idesc = instr_desc<C::kTileM, BN>(bmn);
         for (int kb = 0; kb < nkb; ++kb) {
           if (!wait_bounded(&full[stage], phase, abort_flag, p.status, kWaitLimitNs, true)) {
             ok = false;
@@ -564,21 +665,25 @@ __global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__
             // B K-major: as A. B MN-major: 16 K-rows = two 8-row groups of 1024 B; 64-column groups
             // (one TMA box each) 8192 B apart.
             const uint64_t db = bmn ? smem_desc(sb + k * 2048, 8192, 1024) : smem_desc(sb + k * 32, 16, 1024);
-            mma_f16(d_tmem, da, db, idesc, (kb > 0 || k > 0) ? 1u : 0u);
+            if constexpr (kPair) mma_f16_pair(d_tmem, da, db, idesc, (kb > 0 || k > 0) ? 1u : 0u);
+            else mma_f16(d_tmem, da, db, idesc, (kb > 0 || k > 0) ? 1u : 0u);
           }
-          mma_commit(&empty[stage]);
+          if constexpr (kPair) mma_commit_pair(&empty[stage]);
+          else mma_commit(&empty[stage]);
           if (++stage == C::kStages) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        mma_commit(&tfull[acc]);
+        if constexpr (kPair) mma_commit_pair(&tfull[acc]);
+        else mma_commit(&tfull[acc]);
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1u;
       }
       // Make sure every MMA this thread issued has completed before tensor memory is freed.
-      mma_commit(drain);
+      if constexpr (kPair) mma_commit_pair_local(drain);
+      else mma_commit(drain);
       wait_bounded(drain, 0, abort_flag, p.status, kDrainLimitNs, false);
     }
   } else {
@@ -587,8 +692,8 @@ __global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__
     int acc = 0;
     uint32_t acc_phase = 0;
     bool bad = false;
-    for (int t = blockIdx.x; t < p.ntiles; t += gridDim.x) {
-      const TileRef tr = tile_at(p, t, BN);
+    for (int t = unit; t < p.ntiles; t += nunits) {
+      const TileRef tr = tile_at(p, t, BN, C::kTileM);
       if (tr.skip) continue;
       bool ok = wait_bounded(&tfull[acc], acc_phase, abort_flag, p.status, kWaitLimitNs, true);
       ok = __all_sync(0xffffffffu, ok);
@@ -596,10 +701,14 @@ __global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__
       tc_fence_after();
       const uint32_t taddr =
           tmem_base + static_cast<uint32_t>(acc * BN) + (static_cast<uint32_t>(quarter * 32) << 16);
-      epilogue_tile<BN>(p, *tr.job, tr.tm, tr.tn, quarter, lane, taddr, epi_stage + (warp - 2) * 4096, bad);
+      epilogue_tile<BN>(p, *tr.job, tr.tm * C::kTileM + static_cast<int>(rank) * kBM, tr.tn, quarter, lane, taddr,
+                        epi_stage + (warp - 2) * 4096, bad);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty[acc]);
+      if (lane == 0) {
+        if constexpr (kPair) mbar_arrive_cluster(map_shared(smem_u32(&tempty[acc]), 0));
+        else mbar_arrive(&tempty[acc]);
+      }
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
@@ -610,8 +719,30 @@ __global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__
   __syncwarp();
   tc_fence_before();
   __syncthreads();
+  if constexpr (kPair) {
+    // After an abort a pair CTA cannot see its own copies land (they signal the leader's barrier):
+    // give any copy still in flight time to finish before shared memory is released.
+    if (*abort_flag) {
+      const unsigned long long t0 = globaltimer();
+      while (globaltimer() - t0 < 2000000ull) __nanosleep(10000);
+    }
+    cluster_sync_all();  // neither CTA leaves while its peer may still signal it
+  }
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem_base, C::kTmemCols);
+  if (warp == 1) {
+    if constexpr (kPair) tmem_dealloc_pair(tmem_base, C::kTmemCols);
+    else tmem_dealloc(tmem_base, C::kTmemCols);
+  }
+}
+
+template <int BN>
+__global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__ GemmLaunch p) {
+  gemm_tc_body<BN, 1>(p);
+}
+
+// CTA pairs: a 256 x 256 output tile per pair, one tcgen05.mma.cta_group::2 stream issued by the leader.
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1) gemm_tc_pair_kernel(const __grid_constant__ GemmLaunch p) {
+  gemm_tc_body<256, 2>(p);
 }
 
 // ---------------------------------------------------------------------------- host side
@@ -662,16 +793,15 @@ bool encode_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t oute
 
 }  // namespace
 
-int gemm_smem_bytes(int bn) { return bn == 256 ? Cfg<256>::kSmemBytes : Cfg<128>::kSmemBytes; }
-
 bool encode_job_maps(GemmJob& job, const void* a, int64_t lda, const void* b, int64_t ldb, bool b_mn_major,
-                     int bn, const char** err) {
+                     int tile, const char** err) {
+  const int b_rows = tile_cols(tile) / tile_ctas(tile);  // rows of the K-major B box one CTA loads
   if (!encode_2d(&job.tmA, a, static_cast<uint64_t>(job.K), static_cast<uint64_t>(job.M),
                  static_cast<uint64_t>(lda) * 2, kBK, kBM, err))
     return false;
   if (!b_mn_major)
     return encode_2d(&job.tmB, b, static_cast<uint64_t>(job.K), static_cast<uint64_t>(job.N),
-                     static_cast<uint64_t>(ldb) * 2, kBK, static_cast<uint32_t>(bn), err);
+                     static_cast<uint64_t>(ldb) * 2, kBK, static_cast<uint32_t>(b_rows), err);
   return encode_2d(&job.tmB, b, static_cast<uint64_t>(job.N), static_cast<uint64_t>(job.K),
                    static_cast<uint64_t>(ldb) * 2, 64, kBK, err);
 }
@@ -699,19 +829,60 @@ bool encode_out_maps(GemmJob& job, const char** err) {
   return true;
 }
 
-cudaError_t launch_gemm(const GemmLaunch& p, int bn, int grid, cudaStream_t stream) {
+int gemm_max_units(int tile, int sms) {
+  if (tile != kTilePair256) return sms;
+  // CTA pairs need two SMs of one GPC each: ask how many such clusters fit at once.
+  static int cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return sms / 2;
+  if (cached[dev] > 0) return cached[dev];
+  if (cudaFuncSetAttribute(gemm_tc_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           Cfg<256, 2>::kSmemBytes) != cudaSuccess) {
+    cudaGetLastError();
+    return sms / 2;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(sms & ~1), 1, 1);
+  cfg.blockDim = dim3(192, 1, 1);
+  cfg.dynamicSmemBytes = Cfg<256, 2>::kSmemBytes;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = 2;
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, gemm_tc_pair_kernel, &cfg) != cudaSuccess || n <= 0) {
+    cudaGetLastError();
+    n = sms / 2;
+  }
+  cached[dev] = std::min(n, sms / 2);
+  return cached[dev];
+}
+
+cudaError_t launch_gemm(const GemmLaunch& p, int tile, int units, cudaStream_t stream) {
   if (p.ntiles <= 0) return cudaSuccess;
   cudaError_t e;
-  if (bn == 256) {
-    e = cudaFuncSetAttribute(gemm_tc_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Cfg<256>::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    gemm_tc_kernel<256><<<grid, 192, Cfg<256>::kSmemBytes, stream>>>(p);
-  } else {
-    e = cudaFuncSetAttribute(gemm_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Cfg<128>::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    gemm_tc_kernel<128><<<grid, 192, Cfg<128>::kSmemBytes, stream>>>(p);
+  switch (tile) {
+    case kTilePair256:
+      e = cudaFuncSetAttribute(gemm_tc_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               Cfg<256, 2>::kSmemBytes);
+      if (e != cudaSuccess) return e;
+      gemm_tc_pair_kernel<<<2 * units, 192, Cfg<256, 2>::kSmemBytes, stream>>>(p);
+      break;
+    case kTileSingle256:
+      e = cudaFuncSetAttribute(gemm_tc_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               Cfg<256, 1>::kSmemBytes);
+      if (e != cudaSuccess) return e;
+      gemm_tc_kernel<256><<<units, 192, Cfg<256, 1>::kSmemBytes, stream>>>(p);
+      break;
+    default:
+      e = cudaFuncSetAttribute(gemm_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               Cfg<128, 1>::kSmemBytes);
+      if (e != cudaSuccess) return e;
+      gemm_tc_kernel<128><<<units, 192, Cfg<128, 1>::kSmemBytes, stream>>>(p);
+      break;
   }
   return cudaGetLastError();
 }

@@ -79,14 +79,24 @@ struct GemmLaunch {
   unsigned* status;
 };
 
-// Launch one grouped GEMM (bn = 128 or 256) on `grid` persistent CTAs.
-cudaError_t launch_gemm(const GemmLaunch& p, int bn, int grid, cudaStream_t stream);
-// Dynamic shared memory each variant needs (host query).
-int gemm_smem_bytes(int bn);
+// Output tile configurations of the GEMM kernel.
+enum TileConfig : int {
+  kTileSingle128 = 0,  // one CTA, 128 x 128 tile (products with N <= 128)
+  kTileSingle256 = 1,  // one CTA, 128 x 256 tile
+  kTilePair256 = 2,    // a CTA pair (cluster of 2, tcgen05 cta_group::2), 256 x 256 tile
+};
+inline int tile_rows(int tile) { return tile == kTilePair256 ? 256 : 128; }
+inline int tile_cols(int tile) { return tile == kTileSingle128 ? 128 : 256; }
+inline int tile_ctas(int tile) { return tile == kTilePair256 ? 2 : 1; }
+
+// Largest number of persistent workers of a tile configuration that fit on the device at once.
+int gemm_max_units(int tile, int sms);
+// Launch one grouped GEMM with `units` persistent workers (CTAs, or CTA pairs for kTilePair256).
+cudaError_t launch_gemm(const GemmLaunch& p, int tile, int units, cudaStream_t stream);
 // Encode the operand tensor maps of a job (host). a/b point to fp16 row-major matrices.
 // b_mn_major selects the K x N storage of Bop. Returns false (with a message) on failure.
 bool encode_job_maps(GemmJob& job, const void* a, int64_t lda, const void* b, int64_t ldb,
-                     bool b_mn_major, int bn, const char** err);
+                     bool b_mn_major, int tile, const char** err);
 // Encode the epilogue maps of a job from its D, D2, W pointers and leading dimensions (host). Sets
 // kJobTmaW when the W map can be built (16-byte aligned base and rows); otherwise the final update
 // falls back to direct stores.
