@@ -7,9 +7,9 @@ POLAR_EXPRESS coefficients) and the fp32 weight update -- one dmuon_muon_step ca
     python bench.py [--gpus N] [--steps K] [--warmup W] [--backend gram|direct] [--layers L]
     python bench.py --impl reference ...   # the CPU float64 oracle on a bounded sample
 
-value = algorithmic Newton-Schulz TFLOP/s of the whole job (symmetric products at half: Gram
-6 m^2 n + 20 m^3 per matrix, direct 15 m^2 n + 5 m^3) over the device-timed region, inputs resident in
-HBM. Every input is larger than L2 (129 MB) except the small Gram matrices, so no flush is inserted.
+value = algorithmic Newton-Schulz TFLOP/s of the whole job (every symmetric product counted at half:
+Gram as implemented 6 m^2 n + 17 m^3 per matrix -- R, Z and S = (aI+Z)R are symmetric, Q is a full
+product --, direct 15 m^2 n + 5 m^3) over the device-timed region, inputs resident in HBM. Every input is larger than L2 (129 MB) except the small Gram matrices, so no flush is inserted.
 e2e = the same metric through the public call with the step's gradients copied in from pinned host
 memory and the per-matrix norms read back, inside the timed region.
 """

@@ -95,10 +95,10 @@ def test_invalid_arguments_rejected_without_device(L):
 def test_flop_counts_closed_form():
     for m, n in ((4096, 4096), (1024, 4096), (4096, 14336), (128, 512), (7, 3)):
         mm, nn = min(m, n), max(m, n)
-        assert dm.gram_flops(m, n) == 6 * mm * mm * nn + 20 * mm ** 3
+        assert dm.gram_flops(m, n) == 6 * mm * mm * nn + 17 * mm ** 3
         assert dm.direct_flops(m, n) == 15 * mm * mm * nn + 5 * mm ** 3
-    # no restart: X X^T + 5 R^2 + 4 Q updates + 4 R updates + output
-    assert dm.gram_flops(10, 20, 5, ()) == 100 * 20 + 5 * 1000 + 4 * 2000 + 4 * 3000 + 2 * 100 * 20
+    # no restart: X X^T + 5 R^2 + 4 Q updates + 4 R updates (two symmetric products) + output
+    assert dm.gram_flops(10, 20, 5, ()) == 100 * 20 + 5 * 1000 + 4 * 2000 + 4 * 2000 + 2 * 100 * 20
 
 
 def test_workspace_size_closed_form(L):
