@@ -41,6 +41,8 @@ def parse():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--backend", default="gram", choices=["gram", "direct"])
     ap.add_argument("--layers", type=int, default=32)
+    ap.add_argument("--workload", default="llama", choices=["llama", "small"],
+                    help="llama: Llama-3-8B Muon-target set (the headline); small: 2048 x 128x512 + 512 x 512x128")
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline (profiling runs)")
@@ -49,6 +51,14 @@ def parse():
 
 def workload_config(args):
     import workloads
+    if args.workload == "small":
+        shapes = [(f"m{i}", r, c) for i, (r, c) in enumerate(workloads.small_set_shapes())]
+        return shapes, {
+            "workload": "small-set-2560", "matrices": len(shapes), "params": sum(r * c for _, r, c in shapes),
+            "shapes": "2048 x 128x512 + 512 x 512x128", "grad_dtype": "fp32", "state_dtype": "fp32",
+            "backend": args.backend, "coefficients": "YOU", "restarts": [2] if args.backend == "gram" else [],
+            "lr": LR, "beta": BETA, "eps": EPS, "l2": "inputs larger than L2, no flush",
+        }
     shapes = workloads.llama3_8b_shapes(args.layers)
     return shapes, {
         "workload": f"llama3-8b-muon-set-{args.layers}L" if args.layers != 32 else "llama3-8b-muon-set",
@@ -66,6 +76,33 @@ def total_flops(shapes, backend):
     import newton_schulz_momentum_gb300 as dm
     f = dm.gram_flops if backend == "gram" else dm.direct_flops
     return sum(f(r, c) for _, r, c in shapes)
+
+
+# The GEMM's DRAM traffic depends on the kernel and on the planner's tile order.
+GEMM_SOURCES = [os.path.join(ROOT, "newton_schulz_momentum_gb300", "csrc", f) for f in ("gemm_tc.cu", "api.cu")]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gemm_tc_dram_traffic.json")
+
+
+def gemm_source_digest():
+    import hashlib
+    h = hashlib.sha256()
+    for path in GEMM_SOURCES:
+        with open(path, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def measured_traffic(workload, backend):
+    """DRAM bytes per GEMM launch from the committed ncu capture, or None when the capture was taken on
+    another workload or an earlier version of the kernel source."""
+    try:
+        with open(TRAFFIC_FILE) as fh:
+            rec = json.load(fh)
+    except Exception:
+        return None
+    if rec.get("kernel_source_sha256") != gemm_source_digest():
+        return None
+    return rec.get("per_launch_bytes", {}).get(f"{workload}/{backend}")
 
 
 def peaks():
@@ -127,7 +164,7 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def cpu_oracle_sample(shapes, backend, seconds, seed=7):
+def cpu_oracle_sample(shapes, backend, seconds, seed=7, small=False):
     """Time the float64 oracle (as it stands) on whole matrices of the workload's distinct oriented
     shapes, cycling until about `seconds` of CPU work. Returns (TFLOP/s, flops, seconds, sample text)."""
     import numpy as np
@@ -146,16 +183,19 @@ def cpu_oracle_sample(shapes, backend, seconds, seed=7):
     i = 0
     while spent < seconds or not done:
         name, r, c = distinct[i % len(distinct)]
-        g = workloads.round_to_bf16(workloads.gaussian((r, c), 1e-3, seed + i))[0]
+        g = workloads.gaussian((r, c), 1e-3, seed + i)
+        if not small:
+            g = workloads.round_to_bf16(g)[0]
         w = workloads.gaussian((r, c), 0.02, seed + 100 + i)
         m0 = np.zeros((r, c), dtype=np.float32)
+        coeffs = ns64.YOU if small else ns64.POLAR_EXPRESS
         t0 = time.perf_counter()
-        ns64.muon_step(w, g, m0, LR, BETA, ns64.POLAR_EXPRESS, (2,) if backend == "gram" else (), backend, EPS)
+        ns64.muon_step(w, g, m0, LR, BETA, coeffs, (2,) if backend == "gram" else (), backend, EPS)
         spent += time.perf_counter() - t0
         flops += (dm.gram_flops if backend == "gram" else dm.direct_flops)(r, c)
         done.append(f"{name.split('.')[-1]} {r}x{c}")
         i += 1
-        if i >= 3 * len(distinct):
+        if i >= 3 * len(distinct) and not small:
             break
     return flops / spent / 1e12, flops, spent, "whole-matrix oracle Muon steps: " + ", ".join(done)
 
@@ -175,11 +215,11 @@ def run_reference(args):
     shapes, cfg = workload_config(args)
     per_step = max(args.cpu_seconds / 4.0, 1.0)
     for _ in range(args.warmup):
-        cpu_oracle_sample(shapes[:7], args.backend, 0.0)
+        cpu_oracle_sample(shapes[:7], args.backend, 0.0, small=args.workload == "small")
     tflops, flops, secs = [], 0, 0.0
     sample = ""
     for _ in range(args.steps):
-        v, f, s, sample = cpu_oracle_sample(shapes[:7], args.backend, per_step)
+        v, f, s, sample = cpu_oracle_sample(shapes[:7], args.backend, per_step, small=args.workload == "small")
         tflops.append(v)
         flops += f
         secs += s
@@ -262,15 +302,17 @@ def run_native(args):
     gen = torch.Generator(device=dev)
     gen.manual_seed(1234 + rank)
     W, G, M = [], [], []
+    gdtype = torch.float32 if args.workload == "small" else torch.bfloat16
+    coeffs = dm.YOU if args.workload == "small" else dm.POLAR_EXPRESS
     for _, r, c in shapes:
         W.append(torch.randn((r, c), generator=gen, device=dev) * 0.02)
-        G.append((torch.randn((r, c), generator=gen, device=dev) * 1e-3).to(torch.bfloat16))
+        G.append((torch.randn((r, c), generator=gen, device=dev) * 1e-3).to(gdtype))
         M.append(torch.zeros((r, c), dtype=torch.float32, device=dev))
     norms = torch.empty(len(shapes), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
     def step():
-        dm.muon_step(W, G, M, lr=LR, beta=BETA, coeffs=dm.POLAR_EXPRESS, restarts=(2,), backend=args.backend,
+        dm.muon_step(W, G, M, lr=LR, beta=BETA, coeffs=coeffs, restarts=(2,), backend=args.backend,
                      eps=EPS, norms_out=norms, stream=stream)
 
     for _ in range(args.warmup):
@@ -310,10 +352,12 @@ def run_native(args):
     achieved = per_launch_flops / (gemm_ms / max(gemm_n, 1) * 1e-3) / 1e12 if gemm_ms > 0 else None
     launches = sum(n for _, n in kernel_times.values())
     rw_ms = sum(kernel_times[k][0] for k in ("momentum_sumsq", "finalize_norms", "normalize_cast"))
+    # momentum: G (2 B bf16 / 4 B fp32) + M read 4 + M write 4; normalise: M read 4 + X write 2
+    rw_bytes = (2 if gdtype == torch.bfloat16 else 4) + 4 + 4 + 4 + 2
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
-        v, f, s, sample = cpu_oracle_sample(shapes, args.backend, args.cpu_seconds)
+        v, f, s, sample = cpu_oracle_sample(shapes, args.backend, args.cpu_seconds, small=args.workload == "small")
         cpu = {"value": v, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
                "sample": f"{sample} ({f / 1e12:.2f} TFLOP in {s:.1f} s, float64 NumPy)"}
 
@@ -323,7 +367,8 @@ def run_native(args):
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f16", "data": "synthetic", "config": cfg,
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": tc_sust, "unit": "TFLOP/s",
-                         "frac": (achieved / tc_sust) if achieved else None, "traffic": None,
+                         "frac": (achieved / tc_sust) if achieved else None,
+                         "traffic": measured_traffic(cfg["workload"], args.backend),
                          "kernel": "gemm_tc_kernel (tcgen05 fp16, fp32 accumulate)",
                          "peak_source": f"{src} bf16 sustained (fp16 dense rate equals bf16)"},
             "cpu_baseline": cpu,
@@ -332,8 +377,8 @@ def run_native(args):
             "clocks": clocks.summary(),
             "breakdown_ms_per_step": {k: v[0] / args.steps for k, v in kernel_times.items()},
             "launches_per_step": {k: v[1] / args.steps for k, v in kernel_times.items()},
-            "rowwise_hbm": {"bytes_per_step": sum(r * c for _, r, c in shapes) * 16,
-                            "achieved_gbs": (sum(r * c for _, r, c in shapes) * 16 * args.steps / (rw_ms * 1e-3) / 1e9)
+            "rowwise_hbm": {"bytes_per_step": sum(r * c for _, r, c in shapes) * rw_bytes,
+                            "achieved_gbs": (sum(r * c for _, r, c in shapes) * rw_bytes * args.steps / (rw_ms * 1e-3) / 1e9)
                             if rw_ms > 0 else None, "peak_gbs": hbm},
             "ns_tflops_frac_of_peak": value / world / tc_sust,
         }

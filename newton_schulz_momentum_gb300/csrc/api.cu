@@ -489,11 +489,20 @@ int build_plan_host(Plan& pl, const PlanKey& key, const std::vector<const void*>
       const JobSpec& js = ph[j];
       const int tm_n = (js.M + th - 1) / th;
       const int tn_n = (js.N + tw - 1) / tw;
-      for (int tm = 0; tm < tm_n; ++tm)
-        for (int tn = 0; tn < tn_n; ++tn) {
-          if ((js.flags & kJobSymmetric) && tn * tw + tw - 1 < tm * th) continue;
-          pl.tiles.push_back(GemmTile{j, tm, tn, 0});
-        }
+      // Tile order = the order the persistent workers pick tiles up, so it decides which tiles run at the
+      // same time and share operands in L2. Walk the output column-wise within bands of `band` tile rows:
+      // when the whole A operand fits comfortably in L2 (Q, Z, S, R and the small X of these products)
+      // the band is every row, so each column block of B is read from DRAM once while A stays resident;
+      // otherwise bands of 8 rows make the ~76 concurrent tiles a near-square block that shares both
+      // operands.
+      const int64_t a_bytes = static_cast<int64_t>(js.M) * js.K * 2;
+      const int band = a_bytes <= (int64_t(40) << 20) ? tm_n : std::min(tm_n, 8);
+      for (int g0 = 0; g0 < tm_n; g0 += band)
+        for (int tn = 0; tn < tn_n; ++tn)
+          for (int tm = g0; tm < std::min(g0 + band, tm_n); ++tm) {
+            if ((js.flags & kJobSymmetric) && tn * tw + tw - 1 < tm * th) continue;
+            pl.tiles.push_back(GemmTile{j, tm, tn, 0});
+          }
     }
     L.ntiles = static_cast<int>(pl.tiles.size()) - L.first_tile;
     pl.launches.push_back(L);
