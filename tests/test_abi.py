@@ -111,3 +111,20 @@ def test_workspace_size_closed_form(L):
     small = sum(2 * 2 * min(s) * max(s) + 2 * 2 * min(s) ** 2 for s in shapes)
     got = dm.workspace_size(shapes, "direct")
     assert small <= got <= small * 1.001 + (1 << 22)
+
+
+def test_oversized_dimension_rejected(L):
+    c = (ctypes.c_float * 15)(*[1.0] * 15)
+    r = (ctypes.c_int * 1)(2)
+    rc, msg = _status(L, L.dmuon_ns(4096, 1 << 25, 8, c, 5, r, 1, 1, 1e-7, None))
+    assert rc == dm.ERR_UNSUPPORTED and "larger than" in msg
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    """No CPU fallback: without libdmuon.so every call raises."""
+    monkeypatch.setattr(dm, "_lib", None)
+    monkeypatch.setattr(dm, "LIB_PATH", str(tmp_path / "libdmuon.so"))
+    with pytest.raises(dm.LibraryNotBuilt):
+        dm.version()
+    with pytest.raises(dm.LibraryNotBuilt):
+        dm.set_workspace_limit(0)
