@@ -355,6 +355,14 @@ def run_native(args):
     # momentum: G (2 B bf16 / 4 B fp32) + M read 4 + M write 4; normalise: M read 4 + X write 2
     rw_bytes = (2 if gdtype == torch.bfloat16 else 4) + 4 + 4 + 4 + 2
 
+    # dedicated ownership of this matrix set over 8 owner ranks (host-only LPT), timed and its balance
+    layer_of = [int(name.split(".")[1]) if name.startswith("layers.") else 0 for name, _, _ in shapes]
+    t0 = time.perf_counter()
+    _, loads = dm.assign_owners([(r, c) for _, r, c in shapes], 8, layer_of, "gram_flops")
+    owner_us = (time.perf_counter() - t0) * 1e6
+    ownership = {"ranks": 8, "cost": "gram_flops", "max_over_mean_load": max(loads) / (sum(loads) / 8),
+                 "host_us": owner_us}
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
         v, f, s, sample = cpu_oracle_sample(shapes, args.backend, args.cpu_seconds, small=args.workload == "small")
@@ -381,6 +389,7 @@ def run_native(args):
                             "achieved_gbs": (sum(r * c for _, r, c in shapes) * rw_bytes * args.steps / (rw_ms * 1e-3) / 1e9)
                             if rw_ms > 0 else None, "peak_gbs": hbm},
             "ns_tflops_frac_of_peak": value / world / tc_sust,
+            "owner_assignment": ownership,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -173,6 +173,32 @@ DMUON_API int dmuon_momentum_normalize_noalloc(const void* grad, int grad_dtype,
                                                void* cuda_stream);
 
 /*
+ * dmuon_assign_owners -- dedicated ownership: give each of `count` matrices one owner rank out of
+ * `nranks`, balancing the work (DMuon "Core Concepts", section "均衡划分" / "Balanced partition":
+ * dedicate_params() uses LPT with global balance and same-layer spread; the "Newton-Schulz 变体" page,
+ * section "TP 路由", calls it a deterministic LPT inside compute_balanced_assignment).
+ *
+ * Matrices are taken in decreasing cost (ties: lower index first). Each goes to the rank holding the
+ * fewest matrices of its own layer (so a layer's parameters are broadcast from different ranks at
+ * once); among those, to the rank with the least load so far (ties: lower rank). Without layer_ids
+ * this is plain LPT. Host-only: no device is touched.
+ *
+ *   rows, cols   host, `count` sizes (>= 1).
+ *   layer_ids    host, `count` layer indices (>= 0), or NULL for no layer constraint.
+ *   nranks       1 .. 65536.
+ *   cost_model   DMUON_COST_ELEMENTS (rows*cols), DMUON_COST_GRAM_FLOPS (6 m^2 n + 17 m^3 with
+ *                m = min, n = max: five Gram steps, restart [2]) or DMUON_COST_DIRECT_FLOPS
+ *                (15 m^2 n + 5 m^3).
+ *   owner_out    host, `count` ints: the owner rank of each matrix.
+ *   loads_out    host, `nranks` doubles (the summed cost per rank), or NULL.
+ */
+#define DMUON_COST_ELEMENTS 0
+#define DMUON_COST_GRAM_FLOPS 1
+#define DMUON_COST_DIRECT_FLOPS 2
+DMUON_API int dmuon_assign_owners(int count, const int64_t* rows, const int64_t* cols, const int* layer_ids,
+                                  int nranks, int cost_model, int* owner_out, double* loads_out);
+
+/*
  * dmuon_check_status -- synchronise `cuda_stream`, then read and clear the device status word.
  * Returns DMUON_OK, DMUON_ERR_TIMEOUT (a kernel's bounded wait gave up: its results are invalid),
  * DMUON_ERR_NONFINITE (an fp16 intermediate overflowed or was NaN) or DMUON_ERR_CUDA (an

@@ -44,7 +44,9 @@ EXPORTS = (
     "dmuon_ns", "dmuon_muon_step", "dmuon_momentum_normalize", "dmuon_gemm_f16", "dmuon_check_status",
     "dmuon_last_error", "dmuon_version", "dmuon_set_workspace_limit", "dmuon_workspace_size",
     "dmuon_release_workspace", "dmuon_timing_enable", "dmuon_timing_read", "dmuon_momentum_normalize_noalloc",
+    "dmuon_assign_owners",
 )
+COST_MODELS = {"elements": 0, "gram_flops": 1, "direct_flops": 2}
 NOALLOC_MAX_ELEMS = 268435456
 TIMING_CLASSES = ("momentum_sumsq", "finalize_norms", "normalize_cast", "gemm_tc")
 
@@ -88,6 +90,7 @@ def lib():
     L.dmuon_workspace_size.argtypes = [i32, _c_i64p, _c_i64p, i32, ctypes.POINTER(ctypes.c_size_t)]
     L.dmuon_momentum_normalize_noalloc.argtypes = [vp, i32, vp, i64, i64, vp, vp, f32, f32, vp]
     L.dmuon_timing_enable.argtypes = [i32]
+    L.dmuon_assign_owners.argtypes = [i32, _c_i64p, _c_i64p, _c_ip, i32, i32, _c_ip, ctypes.POINTER(ctypes.c_double)]
     L.dmuon_timing_read.argtypes = [ctypes.POINTER(ctypes.c_double), _c_i64p]
     for name in EXPORTS:
         if name not in ("dmuon_last_error", "dmuon_version"):
@@ -245,6 +248,18 @@ def timing_read():
     n = (ctypes.c_int64 * len(TIMING_CLASSES))()
     _check(lib().dmuon_timing_read(ms, n))
     return {c: (ms[i], n[i]) for i, c in enumerate(TIMING_CLASSES)}
+
+
+def assign_owners(shapes, nranks, layer_ids=None, cost="gram_flops"):
+    """Dedicated ownership by LPT (host-only): returns (owner rank per matrix, summed cost per rank)."""
+    n = len(shapes)
+    rows = (ctypes.c_int64 * n)(*[s[0] for s in shapes])
+    cols = (ctypes.c_int64 * n)(*[s[1] for s in shapes])
+    layers = None if layer_ids is None else (ctypes.c_int * n)(*[int(x) for x in layer_ids])
+    owners = (ctypes.c_int * n)()
+    loads = (ctypes.c_double * nranks)()
+    _check(lib().dmuon_assign_owners(n, rows, cols, layers, int(nranks), COST_MODELS[cost], owners, loads))
+    return list(owners), list(loads)
 
 
 def release_workspace():
