@@ -39,7 +39,8 @@ def parse():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
-    ap.add_argument("--backend", default="gram", choices=["gram", "direct"])
+    ap.add_argument("--backend", default="gram", choices=["gram", "direct", "auto"])
+    ap.add_argument("--restarts", default="2", help="comma-separated restart indices for the Gram form ('' for none)")
     ap.add_argument("--layers", type=int, default=32)
     ap.add_argument("--workload", default="llama", choices=["llama", "small"],
                     help="llama: Llama-3-8B Muon-target set (the headline); small: 2048 x 128x512 + 512 x 512x128")
@@ -56,7 +57,8 @@ def workload_config(args):
         return shapes, {
             "workload": "small-set-2560", "matrices": len(shapes), "params": sum(r * c for _, r, c in shapes),
             "shapes": "2048 x 128x512 + 512 x 512x128", "grad_dtype": "fp32", "state_dtype": "fp32",
-            "backend": args.backend, "coefficients": "YOU", "restarts": [2] if args.backend == "gram" else [],
+            "backend": args.backend, "coefficients": "YOU",
+            "restarts": list(restart_list(args)) if args.backend != "direct" else [],
             "lr": LR, "beta": BETA, "eps": EPS, "l2": "inputs larger than L2, no flush",
         }
     shapes = workloads.llama3_8b_shapes(args.layers)
@@ -66,16 +68,23 @@ def workload_config(args):
         "params": sum(r * c for _, r, c in shapes),
         "shapes": "per layer q/o 4096x4096, k/v 1024x4096, gate/up 14336x4096, down 4096x14336",
         "grad_dtype": "bf16", "state_dtype": "fp32", "backend": args.backend,
-        "coefficients": "POLAR_EXPRESS", "restarts": [2] if args.backend == "gram" else [],
+        "coefficients": "POLAR_EXPRESS", "restarts": list(restart_list(args)) if args.backend != "direct" else [],
         "lr": LR, "beta": BETA, "eps": EPS,
         "l2": "inputs larger than L2, no flush",
     }
 
 
-def total_flops(shapes, backend):
+def restart_list(args):
+    return tuple(int(x) for x in args.restarts.split(",") if x.strip() != "")
+
+
+def total_flops(shapes, backend, restarts=(2,)):
     import newton_schulz_momentum_gb300 as dm
-    f = dm.gram_flops if backend == "gram" else dm.direct_flops
-    return sum(f(r, c) for _, r, c in shapes)
+
+    def one(r, c):
+        direct = backend == "direct" or (backend == "auto" and dm.auto_uses_direct(r, c))
+        return dm.direct_flops(r, c) if direct else dm.gram_flops(r, c, 5, restarts)
+    return sum(one(r, c) for _, r, c in shapes)
 
 
 # The GEMM's DRAM traffic depends on the kernel and on the planner's tile order.
@@ -297,7 +306,7 @@ def run_native(args):
     dm.lib()
 
     shapes, cfg = workload_config(args)
-    flops_step = total_flops(shapes, args.backend)
+    flops_step = total_flops(shapes, args.backend, restart_list(args))
     dev = torch.device("cuda", local)
     gen = torch.Generator(device=dev)
     gen.manual_seed(1234 + rank)
@@ -312,7 +321,7 @@ def run_native(args):
     stream = torch.cuda.current_stream(dev)
 
     def step():
-        dm.muon_step(W, G, M, lr=LR, beta=BETA, coeffs=coeffs, restarts=(2,), backend=args.backend,
+        dm.muon_step(W, G, M, lr=LR, beta=BETA, coeffs=coeffs, restarts=restart_list(args), backend=args.backend,
                      eps=EPS, norms_out=norms, stream=stream)
 
     for _ in range(args.warmup):

@@ -58,7 +58,9 @@ typedef enum dmuon_status {
 
 typedef enum dmuon_ns_backend {
   DMUON_NS_DIRECT = 0, /* X <- a X + b (X X^T) X + c (X X^T)^2 X                                 */
-  DMUON_NS_GRAM = 1    /* R = X X^T, Z = b R + c R^2, Q <- Z Q + a Q, R <- (aI+Z) R (aI+Z), Q X   */
+  DMUON_NS_GRAM = 1,   /* R = X X^T, Z = b R + c R^2, Q <- Z Q + a Q, R <- (aI+Z) R (aI+Z), Q X   */
+  DMUON_NS_AUTO = 2    /* per matrix, the one with fewer flops: direct when max < 4/3 min
+                          (direct 15 m^2 n + 5 m^3 against Gram 6 m^2 n + 17 m^3), else Gram      */
 } dmuon_ns_backend;
 
 typedef enum dmuon_dtype { DMUON_F32 = 0, DMUON_BF16 = 1 } dmuon_dtype;
@@ -79,7 +81,7 @@ typedef enum dmuon_dtype { DMUON_F32 = 0, DMUON_BF16 = 1 } dmuon_dtype;
  *   restarts   host, n_restarts ints, strictly increasing, each in [0, steps - 1]; a restart at k
  *              happens before step k (Gram backend only; ignored by the direct backend). May be NULL
  *              when n_restarts == 0. Index 0 is accepted and has no effect.
- *   backend    DMUON_NS_DIRECT or DMUON_NS_GRAM.
+ *   backend    DMUON_NS_DIRECT, DMUON_NS_GRAM or DMUON_NS_AUTO.
  *   eps        added to the Frobenius norm (not to its square); must be >= 0.
  * Intermediates are fp16 with fp32 accumulation. A zero matrix gives a zero output.
  */

@@ -37,7 +37,7 @@ DEFAULT_RESTARTS = (2,)
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_OOM, ERR_CUDA, ERR_TIMEOUT, ERR_NONFINITE = range(7)
 _STATUS_NAMES = {1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "OOM", 4: "CUDA", 5: "TIMEOUT", 6: "NONFINITE"}
-BACKENDS = {"direct": 0, "gram": 1}
+BACKENDS = {"direct": 0, "gram": 1, "auto": 2}
 F32, BF16 = 0, 1
 
 EXPORTS = (
@@ -284,6 +284,12 @@ def gram_flops(m, n, steps=5, restarts=DEFAULT_RESTARTS):
         if k + 1 < steps and (k + 1) not in rs:
             f += 2 * m ** 3
     return f + 2 * m * m * n
+
+
+def auto_uses_direct(m, n):
+    """The auto backend's per-matrix choice: direct when its flops are below Gram's (n < 4m/3)."""
+    m, n = min(m, n), max(m, n)
+    return 3 * n < 4 * m
 
 
 def direct_flops(m, n, steps=5):

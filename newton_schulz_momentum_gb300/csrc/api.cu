@@ -73,6 +73,7 @@ struct PlanKey {
 struct MatInfo {
   int64_t rows, cols, m, n, ldx, ldm;
   bool trans;
+  bool direct;  // this matrix runs the direct iteration (backend direct, or auto where it is cheaper)
   const void* G;
   float* M;
   float* W;
@@ -202,8 +203,9 @@ int current_device(DeviceState** out) {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
 int check_ns_args(const float* coeffs, int steps, const int* restarts, int n_restarts, int backend, float eps) {
-  if (backend != DMUON_NS_DIRECT && backend != DMUON_NS_GRAM)
-    return fail(DMUON_ERR_INVALID_ARG, "backend must be DMUON_NS_DIRECT (0) or DMUON_NS_GRAM (1), got %d", backend);
+  if (backend != DMUON_NS_DIRECT && backend != DMUON_NS_GRAM && backend != DMUON_NS_AUTO)
+    return fail(DMUON_ERR_INVALID_ARG, "backend must be DMUON_NS_DIRECT (0), DMUON_NS_GRAM (1) or DMUON_NS_AUTO (2), got %d",
+                backend);
   if (steps < 1 || steps > DMUON_MAX_STEPS)
     return fail(DMUON_ERR_INVALID_ARG, "steps must be in [1, %d], got %d", DMUON_MAX_STEPS, steps);
   if (!coeffs) return fail(DMUON_ERR_INVALID_ARG, "coeffs is NULL");
@@ -249,7 +251,8 @@ void symmetric_sq(bool* s_sym, bool* q_sym) {
   *q_sym = v == "q" || v == "sq";
 }
 
-void build_gram_phases(Plan& pl, const std::vector<int>& restarts, int steps) {
+void build_gram_phases(Plan& pl, const std::vector<int>& restarts, int steps, const std::vector<int>& idx,
+                       std::vector<std::vector<JobSpec>>& out, std::vector<int>& out_coef) {
   const int nm = static_cast<int>(pl.mats.size());
   bool s_sym = false, q_sym = false;
   symmetric_sq(&s_sym, &q_sym);
@@ -263,13 +266,13 @@ void build_gram_phases(Plan& pl, const std::vector<int>& restarts, int steps) {
 
   auto push = [&](std::vector<JobSpec>&& ph, int coef) {
     if (!ph.empty()) {
-      pl.phases.push_back(std::move(ph));
-      pl.phase_coef.push_back(coef);
+      out.push_back(std::move(ph));
+      out_coef.push_back(coef);
     }
   };
   auto gram_of_x = [&](int coef) {
     std::vector<JobSpec> ph;
-    for (int i = 0; i < nm; ++i) {
+    for (int i : idx) {
       const MatInfo& mi = pl.mats[i];
       ph.push_back(make_job(i, mi.m, mi.m, mi.n, kRecPlain, kJobSymmetric, X[i], mi.ldx, X[i], mi.ldx, kNone, 0,
                             mi.R, mi.ldm));
@@ -282,7 +285,7 @@ void build_gram_phases(Plan& pl, const std::vector<int>& restarts, int steps) {
   for (int k = 0; k < steps; ++k) {
     if (is_restart[k]) {
       std::vector<JobSpec> ph;
-      for (int i = 0; i < nm; ++i) {
+      for (int i : idx) {
         const MatInfo& mi = pl.mats[i];
         ph.push_back(make_job(i, mi.m, mi.n, mi.m, kRecPlain, kJobBMnMajor, Q[i], mi.ldm, X[i], mi.ldx, kNone, 0,
                               Xb[i], mi.ldx));
@@ -294,7 +297,7 @@ void build_gram_phases(Plan& pl, const std::vector<int>& restarts, int steps) {
     }
     {  // Z = b R + c R^2 (and the first Q after a (re)start)
       std::vector<JobSpec> ph;
-      for (int i = 0; i < nm; ++i) {
+      for (int i : idx) {
         const MatInfo& mi = pl.mats[i];
         ph.push_back(make_job(i, mi.m, mi.m, mi.m, kRecZ, kJobSymmetric | (fresh ? kJobD2 : 0), mi.R, mi.ldm, mi.R,
                               mi.ldm, mi.R, mi.ldm, mi.Z, mi.ldm, fresh ? Q[i] : kNone));
@@ -304,7 +307,7 @@ void build_gram_phases(Plan& pl, const std::vector<int>& restarts, int steps) {
     const bool update_r = (k + 1 < steps) && !is_restart[k + 1];
     {
       std::vector<JobSpec> ph;
-      for (int i = 0; i < nm; ++i) {
+      for (int i : idx) {
         const MatInfo& mi = pl.mats[i];
         if (!fresh) {  // Q' = Z Q + a Q
           ph.push_back(make_job(i, mi.m, mi.m, mi.m, kRecAxpy, kJobBMnMajor | q_flag, mi.Z, mi.ldm, Q[i], mi.ldm, Q[i],
@@ -317,11 +320,11 @@ void build_gram_phases(Plan& pl, const std::vector<int>& restarts, int steps) {
       }
       push(std::move(ph), k);
       if (!fresh)
-        for (int i = 0; i < nm; ++i) std::swap(Q[i], Qb[i]);
+        for (int i : idx) std::swap(Q[i], Qb[i]);
     }
     if (update_r) {  // R = S Z + a S (symmetric)
       std::vector<JobSpec> ph;
-      for (int i = 0; i < nm; ++i) {
+      for (int i : idx) {
         const MatInfo& mi = pl.mats[i];
         ph.push_back(make_job(i, mi.m, mi.m, mi.m, kRecAxpy, kJobSymmetric, mi.S, mi.ldm, mi.Z, mi.ldm, mi.S, mi.ldm,
                               mi.R, mi.ldm));
@@ -332,7 +335,7 @@ void build_gram_phases(Plan& pl, const std::vector<int>& restarts, int steps) {
   }
   {  // output: W <- w_alpha W + w_beta (Q X)
     std::vector<JobSpec> ph;
-    for (int i = 0; i < nm; ++i) {
+    for (int i : idx) {
       const MatInfo& mi = pl.mats[i];
       JobSpec j = make_job(i, mi.m, mi.n, mi.m, kRecPlain, kJobBMnMajor | kJobFinal | (mi.trans ? kJobFinalTrans : 0),
                            Q[i], mi.ldm, X[i], mi.ldx, kNone, 0, kNone, 0);
@@ -344,13 +347,14 @@ void build_gram_phases(Plan& pl, const std::vector<int>& restarts, int steps) {
   }
 }
 
-void build_direct_phases(Plan& pl, int steps) {
+void build_direct_phases(Plan& pl, int steps, const std::vector<int>& idx, std::vector<std::vector<JobSpec>>& out,
+                         std::vector<int>& out_coef) {
   const int nm = static_cast<int>(pl.mats.size());
   std::vector<size_t> X(nm), Xb(nm);
   for (int i = 0; i < nm; ++i) X[i] = pl.mats[i].X, Xb[i] = pl.mats[i].Xb;
   for (int k = 0; k < steps; ++k) {
     std::vector<JobSpec> p1, p2, p3;
-    for (int i = 0; i < nm; ++i) {
+    for (int i : idx) {
       const MatInfo& mi = pl.mats[i];
       // A = X X^T (in R), B = b A + c A^2 (in Z)
       p1.push_back(make_job(i, mi.m, mi.m, mi.n, kRecPlain, kJobSymmetric, X[i], mi.ldx, X[i], mi.ldx, kNone, 0, mi.R,
@@ -368,14 +372,13 @@ void build_direct_phases(Plan& pl, int steps) {
         p3.push_back(j);
       }
     }
-    pl.phases.push_back(std::move(p1));
-    pl.phase_coef.push_back(k);
-    pl.phases.push_back(std::move(p2));
-    pl.phase_coef.push_back(k);
-    pl.phases.push_back(std::move(p3));
-    pl.phase_coef.push_back(k);
+    for (auto* ph : {&p1, &p2, &p3}) {
+      if (ph->empty()) continue;
+      out.push_back(std::move(*ph));
+      out_coef.push_back(k);
+    }
     if (k + 1 < steps)
-      for (int i = 0; i < nm; ++i) std::swap(X[i], Xb[i]);
+      for (int i : idx) std::swap(X[i], Xb[i]);
   }
 }
 
@@ -432,9 +435,11 @@ int build_plan_host(Plan& pl, const PlanKey& key, const std::vector<const void*>
   pl.off_partials = lay.take(sizeof(float) * pl.nchunks);
   pl.off_norms = lay.take(sizeof(float) * nm);
   pl.off_inv = lay.take(sizeof(float) * nm);
-  const bool gram = key.backend == DMUON_NS_GRAM;
   for (int i = 0; i < nm; ++i) {
     MatInfo& mi = pl.mats[i];
+    // auto: direct where its flops (15 m^2 n + 5 m^3) are below Gram's (6 m^2 n + 17 m^3), i.e. n < 4m/3.
+    mi.direct = key.backend == DMUON_NS_DIRECT || (key.backend == DMUON_NS_AUTO && 3 * mi.n < 4 * mi.m);
+    const bool gram = !mi.direct;
     if (key.kind == kPlanMomNorm) continue;
     const size_t xbytes = sizeof(__half) * mi.m * mi.ldx;
     const size_t mbytes = sizeof(__half) * mi.m * mi.ldm;
@@ -467,8 +472,27 @@ int build_plan_host(Plan& pl, const PlanKey& key, const std::vector<const void*>
     part += r.part_count;
   }
   if (key.kind != kPlanMomNorm) {
-    if (gram) build_gram_phases(pl, key.restarts, key.steps);
-    else build_direct_phases(pl, key.steps);
+    std::vector<int> idx_gram, idx_direct;
+    for (int i = 0; i < nm; ++i) (pl.mats[i].direct ? idx_direct : idx_gram).push_back(i);
+    std::vector<std::vector<JobSpec>> gp, dp;
+    std::vector<int> gc, dc;
+    if (!idx_gram.empty()) build_gram_phases(pl, key.restarts, key.steps, idx_gram, gp, gc);
+    if (!idx_direct.empty()) build_direct_phases(pl, key.steps, idx_direct, dp, dc);
+    // Both sequences advance step by step; the t-th launch of step k carries the t-th phase of step k of
+    // each (their matrices are disjoint, and each sequence keeps its own order).
+    size_t gi = 0, di = 0;
+    for (int k = 0; k < key.steps; ++k) {
+      std::vector<std::vector<JobSpec>> ga, da;
+      while (gi < gp.size() && gc[gi] == k) ga.push_back(std::move(gp[gi++]));
+      while (di < dp.size() && dc[di] == k) da.push_back(std::move(dp[di++]));
+      for (size_t t = 0; t < std::max(ga.size(), da.size()); ++t) {
+        std::vector<JobSpec> ph;
+        if (t < ga.size()) ph.insert(ph.end(), ga[t].begin(), ga[t].end());
+        if (t < da.size()) ph.insert(ph.end(), da[t].begin(), da[t].end());
+        pl.phases.push_back(std::move(ph));
+        pl.phase_coef.push_back(k);
+      }
+    }
   }
   // Tiles: per launch, jobs in decreasing K (longest first), tiles row-major within a job.
   size_t njobs = 0;
@@ -673,7 +697,7 @@ int dmuon_ns(float* x, int64_t m, int64_t n, const float* coeffs, int steps, con
     key.backend = backend;
     key.steps = steps;
     key.gdtype = 0;
-    if (backend == DMUON_NS_GRAM) key.restarts.assign(restarts, restarts + n_restarts);
+    if (backend != DMUON_NS_DIRECT) key.restarts.assign(restarts, restarts + n_restarts);
     key.rows = {m};
     key.cols = {n};
     key.ptrs = {reinterpret_cast<uintptr_t>(x)};
@@ -704,7 +728,7 @@ int dmuon_muon_step(int count, float* const* params, const void* const* grads, i
     key.backend = backend;
     key.steps = steps;
     key.gdtype = grad_dtype;
-    if (backend == DMUON_NS_GRAM) key.restarts.assign(restarts, restarts + n_restarts);
+    if (backend != DMUON_NS_DIRECT) key.restarts.assign(restarts, restarts + n_restarts);
     key.rows.assign(rows, rows + count);
     key.cols.assign(cols, cols + count);
     std::vector<const void*> G(count);
@@ -880,7 +904,8 @@ int dmuon_workspace_size(int count, const int64_t* rows, const int64_t* cols, in
     if (!bytes_out) return fail(DMUON_ERR_INVALID_ARG, "bytes_out is NULL");
     int st = check_matrix_list(count, rows, cols);
     if (st != DMUON_OK) return st;
-    if (backend != DMUON_NS_DIRECT && backend != DMUON_NS_GRAM) return fail(DMUON_ERR_INVALID_ARG, "bad backend");
+    if (backend != DMUON_NS_DIRECT && backend != DMUON_NS_GRAM && backend != DMUON_NS_AUTO)
+      return fail(DMUON_ERR_INVALID_ARG, "bad backend");
     PlanKey key;
     key.kind = kPlanMuon;
     key.backend = backend;

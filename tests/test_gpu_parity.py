@@ -162,6 +162,24 @@ def test_ns_deterministic(dm):
     assert np.array_equal(a, b)
 
 
+def test_auto_backend_picks_per_matrix(dm):
+    """auto runs direct where it needs fewer flops (n < 4m/3: square-ish) and Gram elsewhere, in the same
+    grouped launches; each matrix must match the oracle for the form it ran."""
+    shapes = [(384, 384), (256, 1024), (1024, 300), (500, 600), (96, 520), (640, 640)]
+    W = [workloads.gaussian(s, 0.02, 700 + i) for i, s in enumerate(shapes)]
+    G = [workloads.gaussian(s, 1.0, 800 + i) for i, s in enumerate(shapes)]
+    Wd = [cuda(w) for w in W]
+    Md = [torch.zeros(s, dtype=torch.float32, device="cuda") for s in shapes]
+    dm.muon_step(Wd, [cuda(g) for g in G], Md, lr=0.02, beta=0.95, coeffs=dm.YOU, restarts=(2,), backend="auto")
+    dm.check_status()
+    for i, s in enumerate(shapes):
+        form = "direct" if dm.auto_uses_direct(*s) else "gram"
+        ref = muon_ref(W[i], G[i], np.zeros(s), 0.02, 0.95, ns64.YOU, (2,), form)
+        assert check_update(W[i], Wd[i].cpu().numpy(), ref, 0.02) <= TOL_NS, (s, form)
+    assert dm.auto_uses_direct(384, 384) and dm.auto_uses_direct(500, 600)
+    assert not dm.auto_uses_direct(256, 1024) and not dm.auto_uses_direct(1024, 300)
+
+
 # ------------------------------------------------------------------------------- closed-form matrices
 
 
