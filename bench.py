@@ -320,9 +320,12 @@ def run_native(args):
     norms = torch.empty(len(shapes), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
+    muon = dm.MuonStep(W, G, M, coeffs=coeffs, restarts=restart_list(args), backend=args.backend, eps=EPS,
+                       norms_out=norms)
+    cuda_stream = stream.cuda_stream
+
     def step():
-        dm.muon_step(W, G, M, lr=LR, beta=BETA, coeffs=coeffs, restarts=restart_list(args), backend=args.backend,
-                     eps=EPS, norms_out=norms, stream=stream)
+        muon(lr=LR, beta=BETA, stream=cuda_stream)
 
     for _ in range(args.warmup):
         step()

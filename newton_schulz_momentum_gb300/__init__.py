@@ -185,6 +185,44 @@ def muon_step(params: Sequence, grads: Sequence, momenta: Sequence, lr=0.02, bet
                                  float(beta), c, steps, r, nr, _backend(backend), float(eps), _stream(stream)))
 
 
+class MuonStep:
+    """A prepared dmuon_muon_step over fixed tensors: validation and pointer marshalling happen once, so
+    each step() is one C call (what a training loop does every iteration with the same buffers).
+
+        step = MuonStep(params, grads, momenta, coeffs=POLAR_EXPRESS, restarts=(2,), backend="gram")
+        step(lr=0.02, beta=0.95)          # enqueued on the current CUDA stream
+    """
+
+    def __init__(self, params, grads, momenta, coeffs=POLAR_EXPRESS, restarts=DEFAULT_RESTARTS, backend="gram",
+                 eps=1e-7, norms_out=None):
+        n = len(params)
+        if not (len(grads) == len(momenta) == n) or n == 0:
+            raise ValueError("params, grads and momenta must be non-empty lists of equal length")
+        for w, g, m in zip(params, grads, momenta):
+            if w.shape != g.shape or w.shape != m.shape or w.dim() != 2:
+                raise ValueError("each param, grad and momentum must be a 2-D tensor of the same shape")
+            if not (w.is_contiguous() and g.is_contiguous() and m.is_contiguous()):
+                raise ValueError("tensors must be contiguous")
+        self._keep = (list(params), list(grads), list(momenta), norms_out)  # keep the buffers alive
+        self._n = n
+        self._P = (ctypes.c_void_p * n)(*[_ptr(t) for t in params])
+        self._G = (ctypes.c_void_p * n)(*[_ptr(t) for t in grads])
+        self._M = (ctypes.c_void_p * n)(*[_ptr(t) for t in momenta])
+        self._rows = (ctypes.c_int64 * n)(*[t.shape[0] for t in params])
+        self._cols = (ctypes.c_int64 * n)(*[t.shape[1] for t in params])
+        self._gdtype = _grad_dtype(grads)
+        self._coeffs, self._steps = _coeff_array(coeffs)
+        self._restarts, self._nr = _int_array(restarts)
+        self._backend = _backend(backend)
+        self._eps = float(eps)
+        self._norms = _ptr(norms_out)
+
+    def __call__(self, lr=0.02, beta=0.95, stream=None):
+        _check(lib().dmuon_muon_step(self._n, self._P, self._G, self._gdtype, self._M, self._rows, self._cols,
+                                     self._norms, float(lr), float(beta), self._coeffs, self._steps, self._restarts,
+                                     self._nr, self._backend, self._eps, _stream(stream)))
+
+
 def momentum_normalize(grads, momenta, x_out, norms_out, beta=0.95, eps=1e-7, stream=None):
     """M <- beta M + G (grads may be None), norms_out[i] = ||M_i||, x_out[i] = fp16(M_i / (||M_i|| + eps)),
     oriented so rows <= cols."""

@@ -111,6 +111,11 @@ struct Plan {
   std::vector<GemmJob> jobs;
   std::vector<GemmTile> tiles;
   std::vector<LaunchRec> launches;
+  // Fused small-matrix path (every matrix m <= 128, n <= 512): one ns_small launch instead of phases.
+  bool small_fused = false;
+  unsigned restart_mask = 0;
+  size_t off_small = 0;
+  std::vector<SmallJob> small_jobs;
 };
 
 struct Layout {
@@ -382,19 +387,21 @@ void build_direct_phases(Plan& pl, int steps, const std::vector<int>& idx, std::
   }
 }
 
-// Tile configuration of a launch: 128 x 128 single-CTA tiles when every product is at most 128 wide,
-// otherwise 256 x 256 tiles on CTA pairs (DMUON_GEMM_TILE=single selects 128 x 256 single-CTA tiles).
-int pick_tile(int max_n) {
+// Tile configuration of a launch: 128 x 128 single-CTA tiles when every product is at most 128 wide;
+// 128 x 256 single-CTA tiles when every product has at most 128 rows (a 256-row pair tile would be half
+// empty); otherwise 256 x 256 tiles on CTA pairs (DMUON_GEMM_TILE=single selects 128 x 256 tiles).
+int pick_tile(int max_m, int max_n) {
   if (max_n <= 128) return kTileSingle128;
+  if (max_m <= 128) return kTileSingle256;
   const char* env = getenv("DMUON_GEMM_TILE");
   if (env && strcmp(env, "single") == 0) return kTileSingle256;
   return kTilePair256;
 }
 
 int launch_tile(const std::vector<JobSpec>& ph) {
-  int max_n = 0;
-  for (const JobSpec& j : ph) max_n = std::max(max_n, j.N);
-  return pick_tile(max_n);
+  int max_m = 0, max_n = 0;
+  for (const JobSpec& j : ph) max_m = std::max(max_m, j.M), max_n = std::max(max_n, j.N);
+  return pick_tile(max_m, max_n);
 }
 
 // Host-side plan: matrix layout, workspace offsets, phases, tiles. No device calls.
@@ -435,6 +442,17 @@ int build_plan_host(Plan& pl, const PlanKey& key, const std::vector<const void*>
   pl.off_partials = lay.take(sizeof(float) * pl.nchunks);
   pl.off_norms = lay.take(sizeof(float) * nm);
   pl.off_inv = lay.take(sizeof(float) * nm);
+  // Every matrix small enough for the fused kernel: one launch runs the whole iteration
+  // (DMUON_SMALL_FUSED=0 keeps the phase-by-phase grouped launches instead).
+  {
+    const char* env = getenv("DMUON_SMALL_FUSED");
+    bool all_small = key.kind != kPlanMomNorm && !(env && strcmp(env, "0") == 0);
+    for (int i = 0; i < nm && all_small; ++i)
+      all_small = pl.mats[i].m <= kSmallMaxM && pl.mats[i].n <= kSmallMaxN;
+    pl.small_fused = all_small;
+    for (int r : key.restarts)
+      if (r > 0 && r < key.steps) pl.restart_mask |= 1u << r;
+  }
   for (int i = 0; i < nm; ++i) {
     MatInfo& mi = pl.mats[i];
     // auto: direct where its flops (15 m^2 n + 5 m^3) are below Gram's (6 m^2 n + 17 m^3), i.e. n < 4m/3.
@@ -443,6 +461,10 @@ int build_plan_host(Plan& pl, const PlanKey& key, const std::vector<const void*>
     if (key.kind == kPlanMomNorm) continue;
     const size_t xbytes = sizeof(__half) * mi.m * mi.ldx;
     const size_t mbytes = sizeof(__half) * mi.m * mi.ldm;
+    if (pl.small_fused) {  // the fused kernel keeps every other operand on chip
+      mi.X = lay.take(xbytes);
+      continue;
+    }
     mi.X = lay.take(xbytes);
     mi.Xb = lay.take(xbytes);
     mi.R = lay.take(mbytes);
@@ -471,7 +493,9 @@ int build_plan_host(Plan& pl, const PlanKey& key, const std::vector<const void*>
     r.part_count = static_cast<int>(pl.chunk_prefix[i + 1] - pl.chunk_prefix[i]);
     part += r.part_count;
   }
-  if (key.kind != kPlanMomNorm) {
+  if (pl.small_fused) {
+    pl.off_small = lay.take(sizeof(SmallJob) * nm, 256);
+  } else if (key.kind != kPlanMomNorm) {
     std::vector<int> idx_gram, idx_direct;
     for (int i = 0; i < nm; ++i) (pl.mats[i].direct ? idx_direct : idx_gram).push_back(i);
     std::vector<std::vector<JobSpec>> gp, dp;
@@ -585,6 +609,19 @@ int bind_plan(DeviceState& ds, Plan& pl, cudaStream_t stream) {
       pl.jobs.push_back(j);
     }
   }
+  if (pl.small_fused) {
+    pl.small_jobs.assign(pl.mats.size(), SmallJob{});
+    for (size_t i = 0; i < pl.mats.size(); ++i) {
+      const MatInfo& mi = pl.mats[i];
+      std::memset(&pl.small_jobs[i], 0, sizeof(SmallJob));
+      const char* err = nullptr;
+      if (!encode_small_job(pl.small_jobs[i], static_cast<const __half*>(at(mi.X)), mi.ldx, mi.W, mi.cols,
+                            static_cast<int>(mi.m), static_cast<int>(mi.n), mi.trans, mi.direct, &err))
+        return fail(DMUON_ERR_CUDA, "%s", err);
+    }
+    DM_CUDA(cudaMemcpyAsync(base + pl.off_small, pl.small_jobs.data(), sizeof(SmallJob) * pl.small_jobs.size(),
+                            cudaMemcpyHostToDevice, stream), "upload small-matrix jobs");
+  }
   DM_CUDA(cudaMemcpyAsync(base + pl.off_rowmats, pl.rowmats.data(), sizeof(RowMat) * pl.rowmats.size(),
                           cudaMemcpyHostToDevice, stream), "upload matrix table");
   DM_CUDA(cudaMemcpyAsync(base + pl.off_chunk, pl.chunk_prefix.data(), sizeof(int64_t) * pl.chunk_prefix.size(),
@@ -619,6 +656,20 @@ int run_plan(DeviceState& ds, const Plan& pl, const float* coeffs, float lr, flo
           "momentum/sum-of-squares launch");
   DM_CUDA(timed(1, stream, [&] { return launch_finalize_norms(rl, stream); }), "norm launch");
   DM_CUDA(timed(2, stream, [&] { return launch_normalize_cast(rl, pl.ncast, stream); }), "normalise/cast launch");
+  if (pl.small_fused) {
+    SmallLaunch sl;
+    std::memset(&sl, 0, sizeof(sl));
+    sl.jobs = reinterpret_cast<const SmallJob*>(base + pl.off_small);
+    sl.njobs = static_cast<int>(pl.mats.size());
+    sl.steps = pl.key.steps;
+    sl.restart_mask = pl.restart_mask;
+    for (int k = 0; k < 3 * pl.key.steps; ++k) sl.coef[k] = coeffs[k];
+    sl.w_alpha = pl.key.kind == kPlanNs ? 0.f : 1.f;
+    sl.w_beta = pl.key.kind == kPlanNs ? 1.f : -lr;
+    sl.status = ds.status;
+    DM_CUDA(timed(3, stream, [&] { return launch_ns_small(sl, ds.sms, stream); }), "small-matrix kernel launch");
+    return DMUON_OK;
+  }
   const GemmJob* jobs = reinterpret_cast<const GemmJob*>(base + pl.off_jobs);
   const GemmTile* tiles = reinterpret_cast<const GemmTile*>(base + pl.off_tiles);
   for (const LaunchRec& L : pl.launches) {
@@ -811,7 +862,7 @@ int dmuon_gemm_f16(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, 
     DeviceState* ds = nullptr;
     int st = current_device(&ds);
     if (st != DMUON_OK) return st;
-    const int tile = pick_tile(static_cast<int>(N));
+    const int tile = pick_tile(static_cast<int>(M), static_cast<int>(N));
     GemmLaunch gl;
     std::memset(&gl, 0, sizeof(gl));
     GemmJob& j = gl.single;

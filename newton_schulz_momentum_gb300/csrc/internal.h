@@ -102,6 +102,45 @@ bool encode_job_maps(GemmJob& job, const void* a, int64_t lda, const void* b, in
 // falls back to direct stores.
 bool encode_out_maps(GemmJob& job, const char** err);
 
+// Encode a 2-D tensor map (host): `inner` contiguous elements per row, `outer` rows `row_bytes` apart.
+bool encode_tensor_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
+                      uint32_t box_inner, uint32_t box_outer, CUtensorMapDataType dtype, CUtensorMapSwizzle swizzle,
+                      const char** err);
+
+// ------------------------------------------------------------------------------------------------
+// Fused Newton-Schulz for small matrices (ns_small.cu): m <= 128 rows and n <= 512 columns after
+// orientation. One persistent CTA per SM takes one matrix at a time and runs the whole iteration in
+// shared memory and tensor memory, ending with the fused weight update: ONE launch for all matrices.
+// ------------------------------------------------------------------------------------------------
+
+constexpr int kSmallMaxM = 128;
+constexpr int kSmallMaxN = 512;
+
+struct alignas(128) SmallJob {
+  CUtensorMap tmX;  // X (fp16, m x n, ldx), box {64, 128}, 128-byte swizzle
+  CUtensorMap tmW;  // W (fp32, caller orientation), box {32, 32}, 128-byte swizzle (when tma_w)
+  float* W;
+  int64_t ldw;
+  int m, n;
+  int trans;   // W is stored transposed (the matrix was oriented)
+  int tma_w;   // tmW valid; otherwise direct stores
+  int direct;  // 1: direct iteration, 0: Gram iteration
+};
+
+struct SmallLaunch {
+  const SmallJob* jobs;
+  int njobs;
+  int steps;
+  unsigned restart_mask;  // bit k: restart before step k (k > 0)
+  float coef[3 * 16];     // (a, b, c) per step
+  float w_alpha, w_beta;  // W = w_alpha W + w_beta O  (w_alpha 0 or 1)
+  unsigned* status;
+};
+
+bool encode_small_job(SmallJob& job, const __half* X, int64_t ldx, float* W, int64_t ldw, int m, int n, bool trans,
+                      bool direct, const char** err);
+cudaError_t launch_ns_small(const SmallLaunch& p, int sms, cudaStream_t stream);
+
 // ------------------------------------------------------------------------------------------------
 // Row-wise (HBM-bound) kernels (rowwise.cu): momentum + sum of squares, norm finalisation,
 // normalise + fp16 cast (+ transpose to the m <= n orientation).

@@ -241,9 +241,65 @@ def test_muon_step_two_steps(dm, backend):
             Wh[i] = ref["W"]
 
 
+def test_prepared_step_matches_one_shot_call(dm):
+    """MuonStep (pointers marshalled once) must give bit-identical results to muon_step."""
+    shapes = [(96, 520), (520, 96), (200, 200)]
+    W = [workloads.gaussian(s, 0.02, 900 + i) for i, s in enumerate(shapes)]
+    G = [workloads.gaussian(s, 1.0, 910 + i) for i, s in enumerate(shapes)]
+    runs = []
+    for prepared in (False, True):
+        Wd = [cuda(w) for w in W]
+        Gd = [cuda(g) for g in G]
+        Md = [torch.zeros(s, dtype=torch.float32, device="cuda") for s in shapes]
+        if prepared:
+            step = dm.MuonStep(Wd, Gd, Md, coeffs=dm.POLAR_EXPRESS, restarts=(2,), backend="gram")
+            step(lr=0.02, beta=0.95)
+            step(lr=0.02, beta=0.95)
+        else:
+            for _ in range(2):
+                dm.muon_step(Wd, Gd, Md, lr=0.02, beta=0.95, coeffs=dm.POLAR_EXPRESS, restarts=(2,), backend="gram")
+        dm.check_status()
+        runs.append([w.cpu() for w in Wd] + [m.cpu() for m in Md])
+    assert all(torch.equal(a, b) for a, b in zip(*runs))
+
+
+SMALL_SHAPES = [(128, 512), (512, 128), (100, 300), (300, 100), (1, 7), (7, 1), (64, 64), (128, 128), (17, 500),
+                (128, 130), (33, 5)]
+
+
+@pytest.mark.parametrize("backend,restarts", [("gram", (2,)), ("gram", (1, 3)), ("direct", ()), ("auto", (2,))])
+def test_small_fused_kernel_matches_oracle(dm, backend, restarts):
+    """Every matrix with m <= 128 and n <= 512: the whole iteration runs in one fused launch (including W
+    rows that are not 16-byte aligned, written directly instead of by TMA)."""
+    W = [workloads.gaussian(s, 0.02, 1100 + i) for i, s in enumerate(SMALL_SHAPES)]
+    G = [workloads.gaussian(s, 1.0, 1200 + i) for i, s in enumerate(SMALL_SHAPES)]
+    Wd = [cuda(w) for w in W]
+    Md = [torch.zeros(s, dtype=torch.float32, device="cuda") for s in SMALL_SHAPES]
+    dm.timing_enable(True)
+    dm.muon_step(Wd, [cuda(g) for g in G], Md, lr=0.02, beta=0.95, coeffs=dm.YOU, restarts=restarts,
+                 backend=backend)
+    t = dm.timing_read()
+    dm.timing_enable(False)
+    dm.check_status()
+    assert t["gemm_tc"][1] == 1  # one launch for the whole Newton-Schulz part
+    for i, s in enumerate(SMALL_SHAPES):
+        form = backend if backend != "auto" else ("direct" if dm.auto_uses_direct(*s) else "gram")
+        ref = muon_ref(W[i], G[i], np.zeros(s), 0.02, 0.95, ns64.YOU, restarts, form)
+        assert rel(Md[i].cpu().numpy(), ref["M"]) <= TOL_F32
+        assert check_update(W[i], Wd[i].cpu().numpy(), ref, 0.02) <= TOL_NS, (s, form)
+
+
+def test_small_fused_ns_in_place(dm):
+    for shape in ((128, 512), (512, 128), (1, 1), (96, 160)):
+        for backend in ("gram", "direct"):
+            g = workloads.gaussian(shape, 1.0, 1300 + sum(shape))
+            got = run_ns(dm, g, dm.YOU, (2,), backend)
+            assert rel(got, ns64.newton_schulz(g, ns64.YOU, (2,), backend, EPS)) <= TOL_NS
+
+
 def test_small_matrix_set_one_grouped_step(dm):
     """2048 gradients of 128 x 512 plus 512 of 512 x 128, N(0, 1e-3^2), beta 0.95 from zero, Gram with
-    restart [2]: one grouped launch per phase. Graded with YOU; the printed POLAR_EXPRESS set is run too
+    restart [2]: the whole iteration of all 2560 matrices in one fused launch. Graded with YOU; the printed POLAR_EXPRESS set is run too
     and checked only for finiteness and a looser bound (its fp16 error on this shape sits near 3e-2)."""
     shapes = workloads.small_set_shapes()
     G = [workloads.gaussian(s, 1e-3, 1000 + i) for i, s in enumerate(shapes)]
