@@ -42,8 +42,9 @@ def parse():
     ap.add_argument("--backend", default="gram", choices=["gram", "direct", "auto"])
     ap.add_argument("--restarts", default="2", help="comma-separated restart indices for the Gram form ('' for none)")
     ap.add_argument("--layers", type=int, default=32)
-    ap.add_argument("--workload", default="llama", choices=["llama", "small"],
-                    help="llama: Llama-3-8B Muon-target set (the headline); small: 2048 x 128x512 + 512 x 512x128")
+    ap.add_argument("--workload", default="llama", choices=["llama", "small", "adamw"],
+                    help="llama: Llama-3-8B Muon-target set (the headline); small: 2048 x 128x512 + 512 x 512x128; "
+                         "adamw: AdamW over the Llama-3-8B non-Muon parameters")
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline (profiling runs)")
@@ -409,10 +410,66 @@ def run_native(args):
         dist.destroy_process_group()
 
 
+def run_adamw(args):
+    """AdamW over the non-Muon parameters of a Llama-3-8B-shaped model (1.05 G elements, bf16 grads):
+    HBM-bound, reported as GB/s of the bytes each element needs (p, g, m, v in; p, m, v out: 26 B)."""
+    import torch
+
+    import newton_schulz_momentum_gb300 as dm
+    import workloads
+    from newton_schulz_momentum_gb300 import build as dmbuild
+
+    dmbuild.build()
+    dev = torch.device("cuda", 0)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(77)
+    numels = [n for _, n in workloads.llama3_8b_non_muon_numels()]
+    P = [torch.randn(n, generator=gen, device=dev) * 0.02 for n in numels]
+    G = [(torch.randn(n, generator=gen, device=dev) * 1e-3).to(torch.bfloat16) for n in numels]
+    M = [torch.zeros(n, device=dev) for n in numels]
+    V = [torch.zeros(n, device=dev) for n in numels]
+    adam = dm.AdamWStep(P, G, M, V)
+    stream = torch.cuda.current_stream(dev)
+    for t in range(1, args.warmup + 1):
+        adam(t, stream=stream)
+    dm.check_status(stream)
+    dm.timing_enable(True)
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(0) as clocks:
+        start.record(stream)
+        for t in range(args.warmup + 1, args.warmup + args.steps + 1):
+            adam(t, stream=stream)
+        stop.record(stream)
+        torch.cuda.synchronize(dev)
+    kt = dm.timing_read()
+    dm.timing_enable(False)
+    dm.check_status(stream)
+    ms = start.elapsed_time(stop) / args.steps
+    nbytes = sum(numels) * 26
+    hbm, _, _, src = peaks()
+    kms, kn = kt["adamw"]
+    achieved = nbytes / (kms / kn * 1e-3) / 1e9 if kn else None  # one launch per step: bytes / launch time
+    line = {
+        "metric": "AdamW step GB/s, Llama-3-8B non-Muon parameters", "value": nbytes / (ms * 1e-3) / 1e9,
+        "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": "llama3-8b-non-muon-adamw", "tensors": len(numels), "elements": sum(numels),
+                   "grad_dtype": "bf16", "bytes_per_element": 26, "l2": "inputs larger than L2, no flush"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                     "frac": achieved / hbm if achieved else None, "traffic": None, "kernel": "adamw_kernel",
+                     "peak_source": src},
+        "gpu_launches": kn, "clocks": clocks.summary(),
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload == "adamw":
+        run_adamw(args)
     else:
         run_native(args)
 

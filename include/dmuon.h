@@ -201,6 +201,26 @@ DMUON_API int dmuon_assign_owners(int count, const int64_t* rows, const int64_t*
                                   int nranks, int cost_model, int* owner_out, double* loads_out);
 
 /*
+ * dmuon_adamw_step -- AdamW over `count` tensors in one launch, for the parameters that are not Muon
+ * targets (DMuon "Core Concepts", section "1. Dedicated Ownership", step 6 of each training step). The
+ * pages name the optimizer only; this is AdamW with decoupled weight decay in PyTorch's form. For step t:
+ *   p <- p (1 - lr wd);  m <- b1 m + (1 - b1) g;  v <- b2 v + (1 - b2) g^2;
+ *   p <- p - lr / (1 - b1^t) * m / (sqrt(v) / sqrt(1 - b2^t) + eps)
+ *
+ *   params, exp_avg, exp_avg_sq  host arrays of `count` device fp32 pointers (p, m, v; updated in place).
+ *   grads        host array of `count` device pointers, element type grad_dtype (fp32 or bf16).
+ *   numels       host array of `count` element counts (>= 1); tensors are dense.
+ *   step         t >= 1 (the step being taken, counted from 1).
+ *   lr, beta1, beta2, eps, weight_decay are doubles: 1 - beta and the bias corrections are formed in
+ *   double before the kernel sees them in fp32 (1 - fp32(0.999) would be off by 1.3e-5 relative).
+ * The pointer table is cached per device for the same buffers (re-uploaded when they change).
+ */
+DMUON_API int dmuon_adamw_step(int count, float* const* params, const void* const* grads, int grad_dtype,
+                               float* const* exp_avg, float* const* exp_avg_sq, const int64_t* numels, double lr,
+                               double beta1, double beta2, double eps, double weight_decay, int step,
+                               void* cuda_stream);
+
+/*
  * dmuon_check_status -- synchronise `cuda_stream`, then read and clear the device status word.
  * Returns DMUON_OK, DMUON_ERR_TIMEOUT (a kernel's bounded wait gave up: its results are invalid),
  * DMUON_ERR_NONFINITE (an fp16 intermediate overflowed or was NaN) or DMUON_ERR_CUDA (an
@@ -213,10 +233,11 @@ DMUON_API int dmuon_check_status(void* cuda_stream);
  * a pair of CUDA events on the caller's stream around every kernel it launches. dmuon_timing_read
  * waits for the recorded events, writes per kernel class the summed elapsed milliseconds and the
  * number of launches since the previous read (or enable), and clears the record. Classes:
- *   0 momentum + sum of squares, 1 norm finalisation, 2 normalise + fp16 cast, 3 tensor-core GEMM.
+ *   0 momentum + sum of squares, 1 norm finalisation, 2 normalise + fp16 cast, 3 tensor-core GEMM
+ *   (including the fused small-matrix kernel), 4 AdamW.
  * ms_out and launches_out must each hold DMUON_TIMING_CLASSES entries (host memory).
  */
-#define DMUON_TIMING_CLASSES 4
+#define DMUON_TIMING_CLASSES 5
 DMUON_API int dmuon_timing_enable(int on);
 DMUON_API int dmuon_timing_read(double* ms_out, int64_t* launches_out);
 

@@ -44,11 +44,11 @@ EXPORTS = (
     "dmuon_ns", "dmuon_muon_step", "dmuon_momentum_normalize", "dmuon_gemm_f16", "dmuon_check_status",
     "dmuon_last_error", "dmuon_version", "dmuon_set_workspace_limit", "dmuon_workspace_size",
     "dmuon_release_workspace", "dmuon_timing_enable", "dmuon_timing_read", "dmuon_momentum_normalize_noalloc",
-    "dmuon_assign_owners",
+    "dmuon_assign_owners", "dmuon_adamw_step",
 )
 COST_MODELS = {"elements": 0, "gram_flops": 1, "direct_flops": 2}
 NOALLOC_MAX_ELEMS = 268435456
-TIMING_CLASSES = ("momentum_sumsq", "finalize_norms", "normalize_cast", "gemm_tc")
+TIMING_CLASSES = ("momentum_sumsq", "finalize_norms", "normalize_cast", "gemm_tc", "adamw")
 
 
 class LibraryNotBuilt(RuntimeError):
@@ -90,6 +90,8 @@ def lib():
     L.dmuon_workspace_size.argtypes = [i32, _c_i64p, _c_i64p, i32, ctypes.POINTER(ctypes.c_size_t)]
     L.dmuon_momentum_normalize_noalloc.argtypes = [vp, i32, vp, i64, i64, vp, vp, f32, f32, vp]
     L.dmuon_timing_enable.argtypes = [i32]
+    f64 = ctypes.c_double
+    L.dmuon_adamw_step.argtypes = [i32, _c_vpp, _c_vpp, i32, _c_vpp, _c_vpp, _c_i64p, f64, f64, f64, f64, f64, i32, vp]
     L.dmuon_assign_owners.argtypes = [i32, _c_i64p, _c_i64p, _c_ip, i32, i32, _c_ip, ctypes.POINTER(ctypes.c_double)]
     L.dmuon_timing_read.argtypes = [ctypes.POINTER(ctypes.c_double), _c_i64p]
     for name in EXPORTS:
@@ -221,6 +223,43 @@ class MuonStep:
         _check(lib().dmuon_muon_step(self._n, self._P, self._G, self._gdtype, self._M, self._rows, self._cols,
                                      self._norms, float(lr), float(beta), self._coeffs, self._steps, self._restarts,
                                      self._nr, self._backend, self._eps, _stream(stream)))
+
+
+class AdamWStep:
+    """AdamW over fixed tensors (the non-Muon parameters), prepared once; each call is one C call.
+
+        adam = AdamWStep(params, grads, exp_avgs, exp_avg_sqs)
+        adam(step=t, lr=1e-3, betas=(0.9, 0.999), eps=1e-8, weight_decay=0.01)
+    """
+
+    def __init__(self, params, grads, exp_avgs, exp_avg_sqs):
+        n = len(params)
+        if not (len(grads) == len(exp_avgs) == len(exp_avg_sqs) == n) or n == 0:
+            raise ValueError("params, grads, exp_avgs and exp_avg_sqs must be non-empty lists of equal length")
+        for p, g, m, v in zip(params, grads, exp_avgs, exp_avg_sqs):
+            if not (p.numel() == g.numel() == m.numel() == v.numel()):
+                raise ValueError("each param, grad and state must have the same number of elements")
+            if not all(t.is_contiguous() for t in (p, g, m, v)):
+                raise ValueError("tensors must be contiguous")
+        self._keep = (list(params), list(grads), list(exp_avgs), list(exp_avg_sqs))
+        self._n = n
+        self._P = (ctypes.c_void_p * n)(*[_ptr(t) for t in params])
+        self._G = (ctypes.c_void_p * n)(*[_ptr(t) for t in grads])
+        self._M = (ctypes.c_void_p * n)(*[_ptr(t) for t in exp_avgs])
+        self._V = (ctypes.c_void_p * n)(*[_ptr(t) for t in exp_avg_sqs])
+        self._numel = (ctypes.c_int64 * n)(*[t.numel() for t in params])
+        self._gdtype = _grad_dtype(grads)
+
+    def __call__(self, step, lr=1e-3, betas=(0.9, 0.999), eps=1e-8, weight_decay=0.01, stream=None):
+        _check(lib().dmuon_adamw_step(self._n, self._P, self._G, self._gdtype, self._M, self._V, self._numel,
+                                      float(lr), float(betas[0]), float(betas[1]), float(eps), float(weight_decay),
+                                      int(step), _stream(stream)))
+
+
+def adamw_step(params, grads, exp_avgs, exp_avg_sqs, step, lr=1e-3, betas=(0.9, 0.999), eps=1e-8, weight_decay=0.01,
+               stream=None):
+    """One AdamW step over lists of CUDA tensors (fp32 params and states, fp32 or bf16 grads)."""
+    AdamWStep(params, grads, exp_avgs, exp_avg_sqs)(step, lr, betas, eps, weight_decay, stream)
 
 
 def momentum_normalize(grads, momenta, x_out, norms_out, beta=0.95, eps=1e-7, stream=None):

@@ -19,7 +19,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libdmuon.so")
-SOURCES = ("api.cu", "gemm_tc.cu", "ns_small.cu", "rowwise.cu", "noalloc.cu", "partition.cpp")
+SOURCES = ("api.cu", "gemm_tc.cu", "ns_small.cu", "rowwise.cu", "adamw.cu", "noalloc.cu", "partition.cpp")
 ARCH = ("-gencode", "arch=compute_103a,code=sm_103a")
 
 

@@ -128,6 +128,18 @@ struct Layout {
   }
 };
 
+// Cached AdamW table: the tensors and chunk prefix of the last dmuon_adamw_step call on this device.
+struct AdamPlan {
+  std::vector<uintptr_t> key;  // pointers and sizes
+  int gdtype = 0;
+  std::vector<AdamTensor> tensors;
+  std::vector<int64_t> chunk_prefix;
+  char* buf = nullptr;
+  size_t buf_bytes = 0;
+  size_t off_prefix = 0;
+  bool bound = false;
+};
+
 struct DeviceState {
   bool init = false;
   int sms = 0;
@@ -135,6 +147,7 @@ struct DeviceState {
   char* arena = nullptr;
   size_t arena_bytes = 0;
   Plan plan;
+  AdamPlan adam;
 };
 
 std::mutex g_mu;
@@ -907,6 +920,98 @@ int dmuon_check_status(void* cuda_stream) {
   return DMUON_OK;
 }
 
+int dmuon_adamw_step(int count, float* const* params, const void* const* grads, int grad_dtype, float* const* exp_avg,
+                     float* const* exp_avg_sq, const int64_t* numels, double lr, double beta1, double beta2,
+                     double eps, double weight_decay, int step, void* cuda_stream) {
+  try {
+    if (count < 1) return fail(DMUON_ERR_INVALID_ARG, "count must be >= 1");
+    if (!params || !grads || !exp_avg || !exp_avg_sq || !numels)
+      return fail(DMUON_ERR_INVALID_ARG, "params/grads/exp_avg/exp_avg_sq/numels arrays are NULL");
+    if (grad_dtype != DMUON_F32 && grad_dtype != DMUON_BF16)
+      return fail(DMUON_ERR_INVALID_ARG, "grad_dtype must be DMUON_F32 (0) or DMUON_BF16 (1)");
+    if (step < 1) return fail(DMUON_ERR_INVALID_ARG, "step must be >= 1");
+    if (!std::isfinite(lr) || !std::isfinite(weight_decay) || !std::isfinite(eps) || !(eps >= 0.0) ||
+        !(beta1 >= 0.0 && beta1 < 1.0) || !(beta2 >= 0.0 && beta2 < 1.0))
+      return fail(DMUON_ERR_INVALID_ARG, "lr, weight_decay, eps must be finite (eps >= 0) and betas in [0, 1)");
+    std::vector<uintptr_t> key;
+    key.reserve(5 * static_cast<size_t>(count));
+    for (int i = 0; i < count; ++i) {
+      if (!params[i] || !grads[i] || !exp_avg[i] || !exp_avg_sq[i])
+        return fail(DMUON_ERR_INVALID_ARG, "tensor %d has a NULL pointer", i);
+      if (numels[i] < 1) return fail(DMUON_ERR_INVALID_ARG, "tensor %d has no elements", i);
+      key.push_back(reinterpret_cast<uintptr_t>(params[i]));
+      key.push_back(reinterpret_cast<uintptr_t>(grads[i]));
+      key.push_back(reinterpret_cast<uintptr_t>(exp_avg[i]));
+      key.push_back(reinterpret_cast<uintptr_t>(exp_avg_sq[i]));
+      key.push_back(static_cast<uintptr_t>(numels[i]));
+    }
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceState* ds = nullptr;
+    int st = current_device(&ds);
+    if (st != DMUON_OK) return st;
+    cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
+    AdamPlan& ap = ds->adam;
+    if (!(ap.bound && ap.key == key && ap.gdtype == grad_dtype)) {
+      ap.bound = false;
+      ap.key = key;
+      ap.gdtype = grad_dtype;
+      ap.tensors.assign(count, AdamTensor{});
+      ap.chunk_prefix.assign(count + 1, 0);
+      for (int i = 0; i < count; ++i) {
+        AdamTensor& t = ap.tensors[i];
+        t.p = params[i];
+        t.g = grads[i];
+        t.m = exp_avg[i];
+        t.v = exp_avg_sq[i];
+        t.numel = numels[i];
+        t.vec_ok = aligned16(params[i]) && aligned16(grads[i]) && aligned16(exp_avg[i]) && aligned16(exp_avg_sq[i]);
+        ap.chunk_prefix[i + 1] = ap.chunk_prefix[i] + (numels[i] + kAdamChunkElems - 1) / kAdamChunkElems;
+      }
+      if (ap.chunk_prefix[count] >= (int64_t(1) << 31)) return fail(DMUON_ERR_UNSUPPORTED, "too many elements");
+      Layout lay;
+      lay.take(sizeof(AdamTensor) * count);
+      ap.off_prefix = lay.take(sizeof(int64_t) * (count + 1));
+      if (lay.off > ap.buf_bytes) {
+        DM_CUDA(cudaDeviceSynchronize(), "cudaDeviceSynchronize before re-planning");
+        if (ap.buf) cudaFree(ap.buf);
+        ap.buf = nullptr;
+        ap.buf_bytes = 0;
+        if (cudaMalloc(&ap.buf, lay.off) != cudaSuccess) {
+          cudaGetLastError();
+          ap.buf = nullptr;
+          return fail(DMUON_ERR_OOM, "cudaMalloc of %zu bytes for the AdamW table failed", lay.off);
+        }
+        ap.buf_bytes = lay.off;
+      }
+      DM_CUDA(cudaMemcpyAsync(ap.buf, ap.tensors.data(), sizeof(AdamTensor) * count, cudaMemcpyHostToDevice, stream),
+              "upload AdamW table");
+      DM_CUDA(cudaMemcpyAsync(ap.buf + ap.off_prefix, ap.chunk_prefix.data(), sizeof(int64_t) * (count + 1),
+                              cudaMemcpyHostToDevice, stream),
+              "upload AdamW chunk table");
+      ap.bound = true;
+    }
+    AdamLaunch a;
+    std::memset(&a, 0, sizeof(a));
+    a.tensors = reinterpret_cast<const AdamTensor*>(ap.buf);
+    a.ntensors = count;
+    a.chunk_prefix = reinterpret_cast<const int64_t*>(ap.buf + ap.off_prefix);
+    a.gdtype = grad_dtype;
+    a.decay = static_cast<float>(1.0 - lr * weight_decay);
+    a.step_size = static_cast<float>(lr / (1.0 - std::pow(beta1, step)));
+    a.inv_bc2 = static_cast<float>(1.0 / std::sqrt(1.0 - std::pow(beta2, step)));
+    a.beta1 = static_cast<float>(beta1);
+    a.one_minus_beta1 = static_cast<float>(1.0 - beta1);
+    a.beta2 = static_cast<float>(beta2);
+    a.one_minus_beta2 = static_cast<float>(1.0 - beta2);
+    a.eps = static_cast<float>(eps);
+    const int64_t nchunks = ap.chunk_prefix[count];
+    DM_CUDA(timed(4, stream, [&] { return launch_adamw(a, nchunks, stream); }), "AdamW launch");
+    return DMUON_OK;
+  } catch (const std::exception& e) {
+    return fail(DMUON_ERR_OOM, "host exception: %s", e.what());
+  }
+}
+
 int dmuon_timing_enable(int on) {
   std::lock_guard<std::mutex> lock(g_mu);
   for (auto& t : g_timed) {
@@ -990,6 +1095,11 @@ int dmuon_release_workspace(void) {
   ds.arena = nullptr;
   ds.arena_bytes = 0;
   ds.plan = Plan();
+  if (ds.adam.buf) {
+    DM_CUDA(cudaDeviceSynchronize(), "cudaDeviceSynchronize");
+    DM_CUDA(cudaFree(ds.adam.buf), "cudaFree(AdamW table)");
+  }
+  ds.adam = AdamPlan();
   return DMUON_OK;
 }
 

@@ -173,6 +173,32 @@ struct RowLaunch {
   float beta, eps;
 };
 
+// ------------------------------------------------------------------------------------------------
+// Fused AdamW over many tensors (adamw.cu).
+// ------------------------------------------------------------------------------------------------
+
+constexpr int kAdamChunkElems = 16384;  // elements per AdamW CTA (multiple of 8 * 256)
+
+struct AdamTensor {
+  float* p;
+  const void* g;
+  float* m;
+  float* v;
+  int64_t numel;
+  int vec_ok;  // every pointer 16-byte aligned
+  int pad_;
+};
+
+struct AdamLaunch {
+  const AdamTensor* tensors;
+  int ntensors;
+  const int64_t* chunk_prefix;  // ntensors + 1 exclusive prefix of chunks
+  int gdtype;                   // 0 fp32, 1 bf16
+  float decay, step_size, inv_bc2, beta1, one_minus_beta1, beta2, one_minus_beta2, eps;
+};
+
+cudaError_t launch_adamw(const AdamLaunch& a, int64_t nchunks, cudaStream_t stream);
+
 cudaError_t launch_momentum_sumsq(const RowLaunch& p, int64_t nchunks, cudaStream_t stream);
 cudaError_t launch_finalize_norms(const RowLaunch& p, cudaStream_t stream);
 cudaError_t launch_normalize_cast(const RowLaunch& p, int64_t ntiles, cudaStream_t stream);

@@ -31,6 +31,15 @@ LLAMA3_8B_LAYER = (
 )
 
 
+def llama3_8b_non_muon_numels():
+    """[(name, numel)] of the Llama-3-8B parameters that are not Muon targets (AdamW's share): token
+    embeddings and the untied output head (vocabulary 128256 x 4096) and the 65 RMSNorm weights (4096)."""
+    out = [("embed_tokens", 128256 * 4096), ("lm_head", 128256 * 4096), ("norm", 4096)]
+    for i in range(32):
+        out += [(f"layers.{i}.input_layernorm", 4096), (f"layers.{i}.post_attention_layernorm", 4096)]
+    return out
+
+
 def llama3_8b_shapes(layers):
     """[(name, rows, cols)] for `layers` decoder layers (32 for the whole model: 224 matrices)."""
     return [(f"layers.{i}.{name}", r, c) for i in range(layers) for name, r, c in LLAMA3_8B_LAYER]
