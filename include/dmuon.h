@@ -89,6 +89,21 @@ DMUON_API int dmuon_ns(float* x, int64_t m, int64_t n, const float* coeffs, int 
              int n_restarts, int backend, float eps, void* cuda_stream);
 
 /*
+ * dmuon_ns_tp -- dmuon_ns (Gram form) computed the way `shards` tensor-parallel ranks would compute it,
+ * emulated on one GPU ("Newton-Schulz 变体", section "Gram 空间 NS": R is a sum of local Gram matrices,
+ * so exact TP needs one all-reduce of the (m, m) Gram; DMuon "Core Concepts" §5: O(d^2) instead of O(mn)).
+ * The long side of x is split into `shards` column shards (boundaries t * n / shards rounded down to a
+ * multiple of 8). The norm is the fixed-order sum of per-shard sums of squares (the one scalar
+ * all-reduce); every Gram formation R = X X^T (the initial one and each restart's) is the fixed-order sum
+ * of the per-shard products X_t X_t^T, each computed in fp32 (the one m x m all-reduce); the remaining
+ * m x m work and Q X_t are what every rank does locally. Same arguments and output as dmuon_ns.
+ *   shards     1 .. 64; the long side must be at least 16 * shards.
+ * The result equals dmuon_ns up to fp32 summation order and is deterministic run to run.
+ */
+DMUON_API int dmuon_ns_tp(float* x, int64_t m, int64_t n, int shards, const float* coeffs, int steps,
+                          const int* restarts, int n_restarts, float eps, void* cuda_stream);
+
+/*
  * dmuon_muon_step -- one owner-rank Muon update over `count` matrices, batched.
  *   (DMuon "Core Concepts", step "Owner NS update"; Muon(model, lr, ns_backend) on the
  *    "Newton-Schulz 变体" page; momentum-then-orthogonalise of the pwwt.cn post, section 2.)
@@ -233,11 +248,12 @@ DMUON_API int dmuon_check_status(void* cuda_stream);
  * a pair of CUDA events on the caller's stream around every kernel it launches. dmuon_timing_read
  * waits for the recorded events, writes per kernel class the summed elapsed milliseconds and the
  * number of launches since the previous read (or enable), and clears the record. Classes:
- *   0 momentum + sum of squares, 1 norm finalisation, 2 normalise + fp16 cast, 3 tensor-core GEMM
- *   (including the fused small-matrix kernel), 4 AdamW.
+ *   0 momentum + sum of squares (per-shard sums for dmuon_ns_tp), 1 norm finalisation, 2 normalise +
+ *   fp16 cast, 3 tensor-core GEMM (including the fused small-matrix kernel), 4 AdamW, 5 shard Gram
+ *   reduction (dmuon_ns_tp).
  * ms_out and launches_out must each hold DMUON_TIMING_CLASSES entries (host memory).
  */
-#define DMUON_TIMING_CLASSES 5
+#define DMUON_TIMING_CLASSES 6
 DMUON_API int dmuon_timing_enable(int on);
 DMUON_API int dmuon_timing_read(double* ms_out, int64_t* launches_out);
 

@@ -44,11 +44,11 @@ EXPORTS = (
     "dmuon_ns", "dmuon_muon_step", "dmuon_momentum_normalize", "dmuon_gemm_f16", "dmuon_check_status",
     "dmuon_last_error", "dmuon_version", "dmuon_set_workspace_limit", "dmuon_workspace_size",
     "dmuon_release_workspace", "dmuon_timing_enable", "dmuon_timing_read", "dmuon_momentum_normalize_noalloc",
-    "dmuon_assign_owners", "dmuon_adamw_step",
+    "dmuon_assign_owners", "dmuon_adamw_step", "dmuon_ns_tp",
 )
 COST_MODELS = {"elements": 0, "gram_flops": 1, "direct_flops": 2}
 NOALLOC_MAX_ELEMS = 268435456
-TIMING_CLASSES = ("momentum_sumsq", "finalize_norms", "normalize_cast", "gemm_tc", "adamw")
+TIMING_CLASSES = ("momentum_sumsq", "finalize_norms", "normalize_cast", "gemm_tc", "adamw", "tp_reduce")
 
 
 class LibraryNotBuilt(RuntimeError):
@@ -79,6 +79,7 @@ def lib():
     L = ctypes.CDLL(LIB_PATH)
     vp, i64, i32, f32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float
     L.dmuon_ns.argtypes = [vp, i64, i64, _c_fp, i32, _c_ip, i32, i32, f32, vp]
+    L.dmuon_ns_tp.argtypes = [vp, i64, i64, i32, _c_fp, i32, _c_ip, i32, f32, vp]
     L.dmuon_muon_step.argtypes = [i32, _c_vpp, _c_vpp, i32, _c_vpp, _c_i64p, _c_i64p, vp, f32, f32, _c_fp, i32,
                                   _c_ip, i32, i32, f32, vp]
     L.dmuon_momentum_normalize.argtypes = [i32, _c_vpp, i32, _c_vpp, _c_i64p, _c_i64p, _c_vpp, vp, f32, f32, vp]
@@ -153,6 +154,23 @@ def ns(x, coeffs=POLAR_EXPRESS, restarts=DEFAULT_RESTARTS, backend="gram", eps=1
     _check(lib().dmuon_ns(_ptr(x), x.shape[0], x.shape[1], c, steps, r, nr, _backend(backend), float(eps),
                           _stream(stream)))
     return x
+
+
+def ns_tp(x, shards, coeffs=POLAR_EXPRESS, restarts=DEFAULT_RESTARTS, eps=1e-7, stream=None):
+    """ns (Gram form) as `shards` tensor-parallel ranks would compute it: per-shard sums of squares and
+    per-shard fp32 Gram matrices reduced in a fixed order. In place on an fp32 CUDA matrix; returns x."""
+    if x.dim() != 2 or not x.is_contiguous():
+        raise ValueError("x must be a contiguous 2-D tensor")
+    c, steps = _coeff_array(coeffs)
+    r, nr = _int_array(restarts)
+    _check(lib().dmuon_ns_tp(_ptr(x), x.shape[0], x.shape[1], int(shards), c, steps, r, nr, float(eps),
+                             _stream(stream)))
+    return x
+
+
+def shard_bounds(long_side, shards):
+    """Boundaries ns_tp uses along the long side: t * long_side / shards rounded down to a multiple of 8."""
+    return [(t * long_side // shards) // 8 * 8 for t in range(shards)] + [long_side]
 
 
 def _grad_dtype(grads):

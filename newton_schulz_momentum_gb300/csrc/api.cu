@@ -57,15 +57,20 @@ constexpr int64_t kMaxDim = int64_t(1) << 24;
 
 int64_t round_up(int64_t v, int64_t a) { return (v + a - 1) / a * a; }
 
-enum PlanKind { kPlanNs = 0, kPlanMuon = 1, kPlanMomNorm = 2 };
+enum PlanKind { kPlanNs = 0, kPlanMuon = 1, kPlanMomNorm = 2, kPlanNsTp = 3 };
+
+// Host-only flag on a phase's single JobSpec: the phase is the fixed-order sum of a matrix's per-shard
+// fp32 Gram partials into R (not a GEMM).
+constexpr int kJobTpReduce = 1 << 10;
 
 struct PlanKey {
   int kind = -1, backend = 0, steps = 0, gdtype = 0;
+  int shards = 0;  // kPlanNsTp: column shards along the long side
   std::vector<int> restarts;
   std::vector<int64_t> rows, cols;
   std::vector<uintptr_t> ptrs;  // W, G, M, X_out per matrix
   bool operator==(const PlanKey& o) const {
-    return kind == o.kind && backend == o.backend && steps == o.steps && gdtype == o.gdtype &&
+    return kind == o.kind && backend == o.backend && steps == o.steps && gdtype == o.gdtype && shards == o.shards &&
            restarts == o.restarts && rows == o.rows && cols == o.cols && ptrs == o.ptrs;
   }
 };
@@ -79,6 +84,8 @@ struct MatInfo {
   float* W;
   void* xout;  // caller's fp16 X (momentum_normalize only)
   size_t X = kNone, Xb = kNone, R = kNone, Z = kNone, Q = kNone, Qb = kNone, S = kNone;
+  size_t P = kNone;  // kPlanNsTp: `shards` fp32 planes of m x ldp (per-shard Gram partials)
+  int64_t ldp = 0;
 };
 
 // One product in a phase; operands are arena offsets (kNone = unused), resolved when bound.
@@ -90,10 +97,13 @@ struct JobSpec {
   int64_t lda, ldb, lde, ldd;
   float* W;
   int64_t ldw;
+  size_t w_off = kNone;  // W inside the workspace (per-shard Gram partials) instead of a caller pointer
 };
 
 struct LaunchRec {
   int first_job, njobs, first_tile, ntiles, tile, coef;
+  int tp_reduce = 0;  // 1: not a GEMM but the reduction of per-shard Gram partials (tp_mat's)
+  int tp_mat = 0;
 };
 
 struct Plan {
@@ -116,6 +126,9 @@ struct Plan {
   unsigned restart_mask = 0;
   size_t off_small = 0;
   std::vector<SmallJob> small_jobs;
+  // Tensor-parallel emulation (kPlanNsTp): shard boundaries along the long side.
+  std::vector<int64_t> shard_bounds;
+  int tp_slabs = 0;
 };
 
 struct Layout {
@@ -289,6 +302,30 @@ void build_gram_phases(Plan& pl, const std::vector<int>& restarts, int steps, co
     }
   };
   auto gram_of_x = [&](int coef) {
+    if (pl.key.shards > 0) {
+      // Tensor-parallel form: each shard's X_t X_t^T as a full fp32 product into its own plane (what one
+      // rank computes locally), then their fixed-order sum into R (the one all-reduce of the m x m Gram).
+      std::vector<JobSpec> ph, red;
+      for (int i : idx) {
+        const MatInfo& mi = pl.mats[i];
+        for (int t = 0; t < pl.key.shards; ++t) {
+          const int64_t c0 = pl.shard_bounds[t], c1 = pl.shard_bounds[t + 1];
+          const size_t xo = X[i] + static_cast<size_t>(c0) * sizeof(__half);
+          JobSpec j = make_job(i, mi.m, mi.m, static_cast<int>(c1 - c0), kRecPlain, kJobFinal, xo, mi.ldx, xo, mi.ldx,
+                               kNone, 0, kNone, 0);
+          j.W = nullptr;
+          j.w_off = mi.P + static_cast<size_t>(t) * mi.m * mi.ldp * sizeof(float);
+          j.ldw = mi.ldp;
+          ph.push_back(j);
+        }
+        JobSpec r = make_job(i, mi.m, mi.m, pl.key.shards, kRecPlain, kJobTpReduce, kNone, 0, kNone, 0, mi.P, mi.ldp,
+                             mi.R, mi.ldm);
+        red.push_back(r);
+      }
+      push(std::move(ph), coef);
+      push(std::move(red), coef);
+      return;
+    }
     std::vector<JobSpec> ph;
     for (int i : idx) {
       const MatInfo& mi = pl.mats[i];
@@ -452,14 +489,23 @@ int build_plan_host(Plan& pl, const PlanKey& key, const std::vector<const void*>
   pl.ncast = pl.tile_prefix[nm];
   if (pl.nchunks >= (int64_t(1) << 31) || pl.ncast >= (int64_t(1) << 31))
     return fail(DMUON_ERR_UNSUPPORTED, "too many elements in one call");
-  pl.off_partials = lay.take(sizeof(float) * pl.nchunks);
+  int64_t npartials = pl.nchunks;
+  if (key.kind == kPlanNsTp) {
+    // Shards along the long side, boundaries on multiples of 8 columns (16-byte aligned for TMA).
+    const int64_t N = pl.mats[0].n;
+    pl.shard_bounds.assign(key.shards + 1, N);
+    for (int t = 0; t < key.shards; ++t) pl.shard_bounds[t] = (static_cast<int64_t>(t) * N / key.shards) / 8 * 8;
+    pl.tp_slabs = static_cast<int>((pl.mats[0].m + kShardSlab - 1) / kShardSlab);
+    npartials = std::max<int64_t>(npartials, static_cast<int64_t>(key.shards) * pl.tp_slabs);
+  }
+  pl.off_partials = lay.take(sizeof(float) * npartials);
   pl.off_norms = lay.take(sizeof(float) * nm);
   pl.off_inv = lay.take(sizeof(float) * nm);
   // Every matrix small enough for the fused kernel: one launch runs the whole iteration
   // (DMUON_SMALL_FUSED=0 keeps the phase-by-phase grouped launches instead).
   {
     const char* env = getenv("DMUON_SMALL_FUSED");
-    bool all_small = key.kind != kPlanMomNorm && !(env && strcmp(env, "0") == 0);
+    bool all_small = key.kind != kPlanMomNorm && key.kind != kPlanNsTp && !(env && strcmp(env, "0") == 0);
     for (int i = 0; i < nm && all_small; ++i)
       all_small = pl.mats[i].m <= kSmallMaxM && pl.mats[i].n <= kSmallMaxN;
     pl.small_fused = all_small;
@@ -487,6 +533,10 @@ int build_plan_host(Plan& pl, const PlanKey& key, const std::vector<const void*>
       mi.Qb = lay.take(mbytes);
       mi.S = lay.take(mbytes);
     }
+    if (key.kind == kPlanNsTp) {
+      mi.ldp = round_up(mi.m, 4);
+      mi.P = lay.take(sizeof(float) * key.shards * mi.m * mi.ldp);
+    }
   }
   pl.rowmats.resize(nm);
   int part = 0;
@@ -503,7 +553,8 @@ int build_plan_host(Plan& pl, const PlanKey& key, const std::vector<const void*>
     r.trans = mi.trans ? 1 : 0;
     r.vec_ok = 1;  // pointers are validated 16-byte aligned
     r.part_begin = part;
-    r.part_count = static_cast<int>(pl.chunk_prefix[i + 1] - pl.chunk_prefix[i]);
+    r.part_count = key.kind == kPlanNsTp ? key.shards * pl.tp_slabs
+                                         : static_cast<int>(pl.chunk_prefix[i + 1] - pl.chunk_prefix[i]);
     part += r.part_count;
   }
   if (pl.small_fused) {
@@ -545,6 +596,14 @@ int build_plan_host(Plan& pl, const PlanKey& key, const std::vector<const void*>
     L.tile = launch_tile(ph);
     L.coef = pl.phase_coef[p];
     L.first_tile = static_cast<int>(pl.tiles.size());
+    if (!ph.empty() && (ph[0].flags & kJobTpReduce)) {
+      L.tp_reduce = 1;
+      L.tp_mat = ph[0].mat;
+      L.njobs = 0;
+      L.ntiles = 0;
+      pl.launches.push_back(L);
+      continue;
+    }
     const int th = tile_rows(L.tile), tw = tile_cols(L.tile);
     for (int j = 0; j < L.njobs; ++j) {
       const JobSpec& js = ph[j];
@@ -604,6 +663,7 @@ int bind_plan(DeviceState& ds, Plan& pl, cudaStream_t stream) {
   pl.jobs.clear();
   for (size_t p = 0; p < pl.phases.size(); ++p) {
     const int tile = pl.launches[p].tile;
+    if (pl.launches[p].tp_reduce) continue;  // not a GEMM: no job records
     for (const JobSpec& js : pl.phases[p]) {
       GemmJob j;
       std::memset(&j, 0, sizeof(j));
@@ -612,7 +672,7 @@ int bind_plan(DeviceState& ds, Plan& pl, cudaStream_t stream) {
       j.D = static_cast<__half*>(at(js.d));
       j.D2 = static_cast<__half*>(at(js.d2));
       j.E = static_cast<const __half*>(at(js.e));
-      j.W = js.W;
+      j.W = js.W ? js.W : static_cast<float*>(at(js.w_off));
       j.ldd = js.ldd, j.lde = js.lde, j.ldw = js.ldw;
       j.tiles_n = (js.N + tile_cols(tile) - 1) / tile_cols(tile);
       const char* err = nullptr;
@@ -665,8 +725,24 @@ int run_plan(DeviceState& ds, const Plan& pl, const float* coeffs, float lr, flo
   rl.norms_out = norms_out;
   rl.beta = beta;
   rl.eps = eps;
-  DM_CUDA(timed(0, stream, [&] { return launch_momentum_sumsq(rl, pl.nchunks, stream); }),
-          "momentum/sum-of-squares launch");
+  if (pl.key.kind == kPlanNsTp) {
+    // One sum of squares per shard and row slab; their fixed-order sum is the one scalar all-reduce.
+    const MatInfo& mi = pl.mats[0];
+    ShardSumsqLaunch sl;
+    std::memset(&sl, 0, sizeof(sl));
+    sl.x = mi.M;
+    sl.rows = mi.rows;
+    sl.cols = mi.cols;
+    sl.trans = mi.trans ? 1 : 0;
+    sl.shards = pl.key.shards;
+    sl.slabs = pl.tp_slabs;
+    for (int t = 0; t <= pl.key.shards; ++t) sl.bounds[t] = pl.shard_bounds[t];
+    sl.partials = rl.partials;
+    DM_CUDA(timed(0, stream, [&] { return launch_shard_sumsq(sl, stream); }), "shard sum-of-squares launch");
+  } else {
+    DM_CUDA(timed(0, stream, [&] { return launch_momentum_sumsq(rl, pl.nchunks, stream); }),
+            "momentum/sum-of-squares launch");
+  }
   DM_CUDA(timed(1, stream, [&] { return launch_finalize_norms(rl, stream); }), "norm launch");
   DM_CUDA(timed(2, stream, [&] { return launch_normalize_cast(rl, pl.ncast, stream); }), "normalise/cast launch");
   if (pl.small_fused) {
@@ -685,7 +761,21 @@ int run_plan(DeviceState& ds, const Plan& pl, const float* coeffs, float lr, flo
   }
   const GemmJob* jobs = reinterpret_cast<const GemmJob*>(base + pl.off_jobs);
   const GemmTile* tiles = reinterpret_cast<const GemmTile*>(base + pl.off_tiles);
+  const bool overwrite = pl.key.kind == kPlanNs || pl.key.kind == kPlanNsTp;  // W = O, not W -= lr O
   for (const LaunchRec& L : pl.launches) {
+    if (L.tp_reduce) {
+      const MatInfo& mi = pl.mats[L.tp_mat];
+      TpReduceLaunch tr;
+      tr.P = reinterpret_cast<const float*>(base + mi.P);
+      tr.shards = pl.key.shards;
+      tr.m = mi.m;
+      tr.ldp = mi.ldp;
+      tr.plane = mi.m * mi.ldp;
+      tr.R = reinterpret_cast<__half*>(base + mi.R);
+      tr.ldr = mi.ldm;
+      DM_CUDA(timed(5, stream, [&] { return launch_tp_reduce(tr, stream); }), "shard Gram reduction launch");
+      continue;
+    }
     GemmLaunch gl;
     std::memset(&gl, 0, sizeof(gl));
     gl.jobs = jobs + L.first_job;
@@ -694,8 +784,8 @@ int run_plan(DeviceState& ds, const Plan& pl, const float* coeffs, float lr, flo
     gl.a = coeffs[3 * L.coef + 0];
     gl.b = coeffs[3 * L.coef + 1];
     gl.c = coeffs[3 * L.coef + 2];
-    gl.w_alpha = pl.key.kind == kPlanNs ? 0.f : 1.f;
-    gl.w_beta = pl.key.kind == kPlanNs ? 1.f : -lr;
+    gl.w_alpha = overwrite ? 0.f : 1.f;
+    gl.w_beta = overwrite ? 1.f : -lr;
     gl.status = ds.status;
     const int units = std::min(L.ntiles, gemm_max_units(L.tile, ds.sms));
     DM_CUDA(timed(3, stream, [&] { return launch_gemm(gl, L.tile, units, stream); }), "tensor-core GEMM launch");
@@ -762,6 +852,34 @@ int dmuon_ns(float* x, int64_t m, int64_t n, const float* coeffs, int steps, con
     key.steps = steps;
     key.gdtype = 0;
     if (backend != DMUON_NS_DIRECT) key.restarts.assign(restarts, restarts + n_restarts);
+    key.rows = {m};
+    key.cols = {n};
+    key.ptrs = {reinterpret_cast<uintptr_t>(x)};
+    return plan_and_run(key, {nullptr}, {x}, {x}, {nullptr}, coeffs, 0.f, 0.f, eps, nullptr,
+                        static_cast<cudaStream_t>(cuda_stream));
+  } catch (const std::exception& e) {
+    return fail(DMUON_ERR_OOM, "host exception: %s", e.what());
+  }
+}
+
+int dmuon_ns_tp(float* x, int64_t m, int64_t n, int shards, const float* coeffs, int steps, const int* restarts,
+                int n_restarts, float eps, void* cuda_stream) {
+  try {
+    if (!x) return fail(DMUON_ERR_INVALID_ARG, "x is NULL");
+    if (!aligned16(x)) return fail(DMUON_ERR_INVALID_ARG, "x must be 16-byte aligned");
+    int st = check_matrix_list(1, &m, &n);
+    if (st != DMUON_OK) return st;
+    st = check_ns_args(coeffs, steps, restarts, n_restarts, DMUON_NS_GRAM, eps);
+    if (st != DMUON_OK) return st;
+    if (shards < 1 || shards > kMaxShards) return fail(DMUON_ERR_INVALID_ARG, "shards must be in [1, %d]", kMaxShards);
+    if (std::max(m, n) < 16 * static_cast<int64_t>(shards))
+      return fail(DMUON_ERR_INVALID_ARG, "each shard needs at least 16 columns of the long side");
+    PlanKey key;
+    key.kind = kPlanNsTp;
+    key.backend = DMUON_NS_GRAM;
+    key.steps = steps;
+    key.shards = shards;
+    key.restarts.assign(restarts, restarts + n_restarts);
     key.rows = {m};
     key.cols = {n};
     key.ptrs = {reinterpret_cast<uintptr_t>(x)};

@@ -199,6 +199,35 @@ struct AdamLaunch {
 
 cudaError_t launch_adamw(const AdamLaunch& a, int64_t nchunks, cudaStream_t stream);
 
+// ------------------------------------------------------------------------------------------------
+// Tensor-parallel emulation of the Gram form (rowwise.cu): the matrix split into column shards along
+// its long side, per-shard sums of squares and per-shard Gram matrices reduced in a fixed order.
+// ------------------------------------------------------------------------------------------------
+
+constexpr int kMaxShards = 64;
+constexpr int kShardSlab = 64;  // rows (short side) per shard sum-of-squares CTA
+
+struct ShardSumsqLaunch {
+  const float* x;  // caller matrix, rows x cols fp32
+  int64_t rows, cols;
+  int trans;  // rows > cols: the long side (sharded) is the row index
+  int shards, slabs;
+  int64_t bounds[kMaxShards + 1];  // shard boundaries along the long side
+  float* partials;                 // shards * slabs, shard-major
+};
+
+// R[i][j] = fp16(sum over t of P_t[min(i,j)][max(i,j)]), t = 0 .. shards-1 in order.
+struct TpReduceLaunch {
+  const float* P;  // shards planes of m x ldp fp32
+  int shards;
+  int64_t m, ldp, plane;
+  __half* R;
+  int64_t ldr;
+};
+
+cudaError_t launch_shard_sumsq(const ShardSumsqLaunch& p, cudaStream_t stream);
+cudaError_t launch_tp_reduce(const TpReduceLaunch& p, cudaStream_t stream);
+
 cudaError_t launch_momentum_sumsq(const RowLaunch& p, int64_t nchunks, cudaStream_t stream);
 cudaError_t launch_finalize_norms(const RowLaunch& p, cudaStream_t stream);
 cudaError_t launch_normalize_cast(const RowLaunch& p, int64_t ntiles, cudaStream_t stream);

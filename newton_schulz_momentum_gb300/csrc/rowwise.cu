@@ -222,7 +222,47 @@ __global__ void __launch_bounds__(kThreads) normalize_cast_kernel(const RowLaunc
   }
 }
 
+// Sum of squares of one shard (columns [bounds[t], bounds[t+1]) of the oriented matrix) over one slab of
+// kShardSlab oriented rows. Consecutive threads read consecutive addresses in both orientations.
+__global__ void __launch_bounds__(kThreads) shard_sumsq_kernel(const ShardSumsqLaunch p) {
+  __shared__ float red[kThreads / 32];
+  const int t = blockIdx.y, s = blockIdx.x;
+  const int64_t m = p.trans ? p.cols : p.rows;
+  const int64_t c0 = p.bounds[t], c1 = p.bounds[t + 1];
+  const int64_t r0 = static_cast<int64_t>(s) * kShardSlab, r1 = min(r0 + kShardSlab, m);
+  const int64_t w = c1 - c0, h = r1 - r0;
+  float acc = 0.f;
+  for (int64_t e = threadIdx.x; e < w * h; e += kThreads) {
+    float v;
+    if (!p.trans) v = p.x[(r0 + e / w) * p.cols + c0 + e % w];   // oriented (i, j) = caller (i, j)
+    else v = p.x[(c0 + e / h) * p.cols + r0 + e % h];           // oriented (i, j) = caller (j, i)
+    acc = fmaf(v, v, acc);
+  }
+  const float total = block_sum(acc, red);
+  if (threadIdx.x == 0) p.partials[t * p.slabs + s] = total;
+}
+
+__global__ void __launch_bounds__(kThreads) tp_reduce_kernel(const TpReduceLaunch p) {
+  const int64_t i = blockIdx.x;
+  for (int64_t j = threadIdx.x; j < p.m; j += kThreads) {
+    const int64_t a = min(i, j), b = max(i, j);
+    float acc = 0.f;
+    for (int t = 0; t < p.shards; ++t) acc += p.P[t * p.plane + a * p.ldp + b];
+    p.R[i * p.ldr + j] = __float2half_rn(acc);
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_shard_sumsq(const ShardSumsqLaunch& p, cudaStream_t stream) {
+  shard_sumsq_kernel<<<dim3(static_cast<unsigned>(p.slabs), static_cast<unsigned>(p.shards)), kThreads, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_tp_reduce(const TpReduceLaunch& p, cudaStream_t stream) {
+  tp_reduce_kernel<<<static_cast<unsigned>(p.m), kThreads, 0, stream>>>(p);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_momentum_sumsq(const RowLaunch& p, int64_t nchunks, cudaStream_t stream) {
   if (nchunks <= 0) return cudaSuccess;

@@ -153,3 +153,42 @@ def muon_step(w0, g, m0, lr, beta, coeffs=POLAR_EXPRESS, restarts=DEFAULT_RESTAR
         o = o.T
     w = np.asarray(w0, dtype=np.float64) - lr * o
     return {"M": m, "norm": s, "X": x_oriented, "O": o, "W": w}
+
+
+def gram_by_shards(x, bounds):
+    """Sum over column shards [bounds[t], bounds[t+1]) of X_t X_t^T ("Gram 空间 NS": the Gram matrix is a
+    sum of local Gram matrices, which is what makes tensor parallelism exact with one all-reduce)."""
+    x = np.asarray(x, dtype=np.float64)
+    r = np.zeros((x.shape[0], x.shape[0]))
+    for t in range(len(bounds) - 1):
+        xt = x[:, bounds[t]:bounds[t + 1]]
+        r += xt @ xt.T
+    return r
+
+
+def ns_gram_tp(x, coeffs, restarts, bounds):
+    """ns_gram with every Gram formation (the first and each restart's) taken as gram_by_shards."""
+    x = np.array(x, dtype=np.float64)
+    eye = np.eye(x.shape[0])
+    r = gram_by_shards(x, bounds)
+    q = eye.copy()
+    restart_set = set(int(k) for k in restarts)
+    for k, (a, b, c) in enumerate(coeffs):
+        if k in restart_set and k > 0:
+            x = q @ x
+            r = gram_by_shards(x, bounds)
+            q = eye.copy()
+        z = b * r + c * (r @ r)
+        q = z @ q + a * q
+        r = _gram_update(r, z, a)
+    return q @ x
+
+
+def newton_schulz_tp(g, coeffs, restarts, bounds, eps=1e-7):
+    """Gram NS of g split into column shards of its long side: the squared norm is the sum of per-shard
+    sums of squares, the Gram matrices sums of per-shard products. Returns O with the shape of g."""
+    x, transposed = orient(np.asarray(g, dtype=np.float64))
+    sumsq = sum(float(np.sum(x[:, bounds[t]:bounds[t + 1]] ** 2)) for t in range(len(bounds) - 1))
+    x = x / (np.sqrt(sumsq) + eps)
+    o = ns_gram_tp(x, coeffs, restarts, bounds)
+    return o.T if transposed else o
