@@ -48,6 +48,8 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline (profiling runs)")
+    ap.add_argument("--torch-mm-context", action="store_true",
+                    help="time the same step written with torch.mm (cuBLAS) instead; context only")
     return ap.parse_args()
 
 
@@ -464,10 +466,71 @@ def run_adamw(args):
     print(json.dumps(line), flush=True)
 
 
+def run_torch_mm_context(args):
+    """Context only, not the product path: the same step (momentum, norm, fp16 Gram NS with restart [2],
+    W update) written with torch.mm (cuBLAS fp16 GEMMs, fp32 accumulation) one matrix at a time, timed
+    like the native arm. Prints one JSON line with "impl": "torch-mm-context"."""
+    import torch
+
+    import newton_schulz_momentum_gb300 as dm
+
+    shapes, cfg = workload_config(args)
+    dev = torch.device("cuda", 0)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(1234)
+    W = [torch.randn((r, c), generator=gen, device=dev) * 0.02 for _, r, c in shapes]
+    G = [(torch.randn((r, c), generator=gen, device=dev) * 1e-3).to(torch.bfloat16) for _, r, c in shapes]
+    M = [torch.zeros((r, c), device=dev) for _, r, c in shapes]
+    coeffs = dm.POLAR_EXPRESS
+    restarts = set(restart_list(args))
+
+    def ns(x):
+        eye = torch.eye(x.shape[0], device=dev, dtype=torch.float16)
+        r = x @ x.T
+        q = eye.clone()
+        for k, (a, b, c) in enumerate(coeffs):
+            if k in restarts and k > 0:
+                x = q @ x
+                r = x @ x.T
+                q = eye.clone()
+            z = b * r + c * (r @ r)
+            q = z @ q + a * q
+            if k + 1 < len(coeffs) and (k + 1) not in restarts:
+                w = z + a * eye
+                r = (w @ r) @ w
+        return q @ x
+
+    def step():
+        for w, g, m in zip(W, G, M):
+            m.mul_(BETA).add_(g.float())
+            x = (m / (m.norm() + EPS)).half()
+            t = x.shape[0] > x.shape[1]
+            o = ns(x.T if t else x)
+            w.add_((o.T if t else o).float(), alpha=-LR)
+
+    for _ in range(args.warmup):
+        step()
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    start.record()
+    for _ in range(args.steps):
+        step()
+    stop.record()
+    torch.cuda.synchronize(dev)
+    ms = start.elapsed_time(stop) / args.steps
+    flops = total_flops(shapes, "gram", restart_list(args))
+    print(json.dumps({"impl": "torch-mm-context", "metric": METRIC, "value": flops / (ms * 1e-3) / 1e12,
+                      "unit": UNIT, "ms_per_step": ms, "steps": args.steps, "warmup": args.warmup,
+                      "config": cfg, "note": "cuBLAS fp16 via torch.mm, one matrix at a time; same algorithm "
+                      "and flop count as the native arm; context only"}), flush=True)
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
+    elif args.torch_mm_context:
+        run_torch_mm_context(args)
     elif args.workload == "adamw":
         run_adamw(args)
     else:
