@@ -52,6 +52,8 @@ struct Cfg {
 
 // ---------------------------------------------------------------------------- tile bookkeeping
 
+constexpr int kSingleBand = 8;  // tile rows per raster band of a single-job launch
+
 struct TileRef {
   const GemmJob* job;
   int tm, tn;
@@ -67,9 +69,15 @@ __device__ __forceinline__ TileRef tile_at(const GemmLaunch& p, int t, int bn, i
     r.tn = g.tn;
     r.skip = false;
   } else {
+    // One job: bands of kSingleBand tile rows, walked column by column, so the tiles in flight at
+    // once form a near-square block whose A and B panels stay in L2 together.
     r.job = &p.single;
-    r.tm = t / p.single.tiles_n;
-    r.tn = t - r.tm * p.single.tiles_n;
+    const int tiles_n = p.single.tiles_n;
+    const int g0 = (t / (kSingleBand * tiles_n)) * kSingleBand;
+    const int bh = min(kSingleBand, p.tiles_m - g0);
+    const int u = t - g0 * tiles_n;
+    r.tn = u / bh;
+    r.tm = g0 + (u - r.tn * bh);
     r.skip = (p.single.flags & kJobSymmetric) && (r.tn * bn + bn - 1 < r.tm * tile_m);
   }
   return r;
@@ -326,11 +334,10 @@ __device__ __forceinline__ void gemm_tc_body(const GemmLaunch& p) {
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
-      int issued[C::kStages];
-      uint32_t issued_parity[C::kStages];
-#pragma unroll
-      for (int s = 0; s < C::kStages; ++s) issued[s] = 0, issued_parity[s] = 0;
+      uint32_t issued = 0, issued_parity = 0;  // per ring slot: a copy was issued / with which parity
       bool ok = true;
+      // The leader's full barriers as seen from either CTA of a pair (consecutive 8-byte words).
+      const uint32_t full_leader = kPair ? map_shared(smem_u32(&full[0]), 0) : 0u;
       for (int t = unit; ok && t < p.ntiles; t += nunits) {
         const TileRef tr = tile_at(p, t, BN, C::kTileM);
         if (tr.skip) continue;
@@ -340,7 +347,7 @@ __device__ __forceinline__ void gemm_tc_body(const GemmLaunch& p) {
         const int m0 = tr.tm * C::kTileM + static_cast<int>(rank) * kBM;   // this CTA's 128 rows of A
         const int n0 = tr.tn * BN + static_cast<int>(rank) * C::kBRows;   // this CTA's rows of B
         for (int kb = 0; kb < nkb; ++kb) {
-          if (!wait_bounded(&empty[stage], phase ^ 1u, abort_flag, p.status, kWaitLimitNs, true)) {
+          if (!wait_fast(&empty[stage], phase ^ 1u, abort_flag, p.status)) {
             ok = false;
             break;
           }
@@ -348,7 +355,7 @@ __device__ __forceinline__ void gemm_tc_body(const GemmLaunch& p) {
           const uint32_t sb = sa + C::kABytes;
           if constexpr (kPair) {
             // Both CTAs' copies complete on the leader's full barrier; the leader expects both.
-            const uint32_t bar = map_shared(smem_u32(&full[stage]), 0);
+            const uint32_t bar = full_leader + 8u * static_cast<uint32_t>(stage);
             if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * C::kStageBytes);
             tma_load_2d_pair(sa, &job->tmA, kb * kBK, m0, bar);
             if (!bmn) {
@@ -368,8 +375,8 @@ __device__ __forceinline__ void gemm_tc_body(const GemmLaunch& p) {
               for (int q = 0; q < C::kBRows / 64; ++q) tma_load_2d(sb + q * 8192, &job->tmB, n0 + q * 64, kb * kBK, &full[stage]);
             }
           }
-          issued[stage] = 1;
-          issued_parity[stage] = phase;
+          issued |= 1u << stage;
+          issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
           if (++stage == C::kStages) {
             stage = 0;
             phase ^= 1u;
@@ -379,7 +386,8 @@ __device__ __forceinline__ void gemm_tc_body(const GemmLaunch& p) {
       if (!ok && !kPair) {
         // Aborting: let every copy already issued land before the CTA's shared memory is released.
         for (int s = 0; s < C::kStages; ++s)
-          if (issued[s]) wait_bounded(&full[s], issued_parity[s], abort_flag, p.status, kDrainLimitNs, false);
+          if ((issued >> s) & 1u)
+            wait_bounded(&full[s], (issued_parity >> s) & 1u, abort_flag, p.status, kDrainLimitNs, false);
       }
       // (A pair's copies complete on the leader's barriers; the closing cluster barrier plus the
       // leader's drain keep both CTAs resident until then.)
@@ -403,7 +411,7 @@ __device__ __forceinline__ void gemm_tc_body(const GemmLaunch& p) {
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
         const uint32_t idesc = instr_desc<C::kTileM, BN>(bmn);
         for (int kb = 0; kb < nkb; ++kb) {
-          if (!wait_bounded(&full[stage], phase, abort_flag, p.status, kWaitLimitNs, true)) {
+          if (!wait_fast(&full[stage], phase, abort_flag, p.status)) {
             ok = false;
             break;
           }

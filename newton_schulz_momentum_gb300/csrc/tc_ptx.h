@@ -74,6 +74,12 @@ static __device__ __noinline__ bool wait_bounded(uint64_t* bar, uint32_t parity,
   }
 }
 
+// wait_bounded with its first probe inline: mbarrier.try_wait already suspends the thread for a
+// hardware-defined window, so on the ring's hot path the out-of-line bounded loop is rarely entered.
+__device__ __forceinline__ bool wait_fast(uint64_t* bar, uint32_t parity, volatile int* abort_flag, unsigned* status) {
+  return mbar_try_wait(bar, parity) || wait_bounded(bar, parity, abort_flag, status, kWaitLimitNs, true);
+}
+
 __device__ __forceinline__ void tma_load_2d(uint32_t smem_dst, const CUtensorMap* map, int c0, int c1,
                                             uint64_t* bar) {
   asm volatile(
