@@ -122,6 +122,14 @@ __device__ void epilogue_tile(const GemmLaunch& p, const GemmJob& job, int tile_
   const __half* erow = (job.E != nullptr && s.e != 0.f && row_ok) ? job.E + static_cast<int64_t>(i) * job.lde : nullptr;
   const bool has_e = job.E != nullptr && s.e != 0.f;
   const uint32_t sbuf = smem_u32(stage);
+  const bool scale = s.acc != 1.f;
+  // Overflow / NaN detection without per-element compares: an fp16 (or, for the final output, fp32)
+  // value that is inf or NaN times zero is NaN, so one packed FMA per pair of outputs folds the check into
+  // an accumulator tested once per tile. Columns past N hold zeros (out-of-range operand boxes are
+  // zero-filled by TMA), so they never raise it.
+  const __half2 zero2 = __float2half2_rn(0.f);
+  __half2 chk16 = zero2;
+  float chk32 = 0.f;
 
   // Symmetric outputs: chunks left of the diagonal block are produced by the mirrored stores of other
   // tiles, so this warp starts at its diagonal block (row0 and tn*BN are multiples of 32).
@@ -170,11 +178,11 @@ __device__ void epilogue_tile(const GemmLaunch& p, const GemmJob& job, int tile_
           v[k] = fmaf(s.acc, v[k], s.e * e);
         }
       }
-    } else {
+    } else if (scale) {
 #pragma unroll
       for (int k = 0; k < 32; ++k) v[k] *= s.acc;
     }
-    if (s.diag != 0.f) {
+    if (s.diag != 0.f && j0 == row0) {  // only the block on the diagonal holds elements with j == i
 #pragma unroll
       for (int k = 0; k < 32; ++k)
         if (j0 + k == i) v[k] += s.diag;
@@ -186,7 +194,7 @@ __device__ void epilogue_tile(const GemmLaunch& p, const GemmJob& job, int tile_
 
     if (final_out) {
 #pragma unroll
-      for (int k = 0; k < 32; ++k) bad |= (j0 + k < job.N) && !isfinite(v[k]);
+      for (int k = 0; k < 32; ++k) chk32 = fmaf(v[k], 0.f, chk32);
       if (tma_w) {
         if (lane == 0) bulk_wait_read0();
         __syncwarp();
@@ -228,8 +236,12 @@ __device__ void epilogue_tile(const GemmLaunch& p, const GemmJob& job, int tile_
       continue;
     }
 
+    uint32_t pk[16];  // the chunk's row rounded to fp16, two columns per word
 #pragma unroll
-    for (int k = 0; k < 32; ++k) bad |= (j0 + k < job.N) && !fp16_ok(v[k]);
+    for (int q = 0; q < 16; ++q) {
+      pk[q] = pack_half2(v[2 * q], v[2 * q + 1]);
+      chk16 = __hfma2(*reinterpret_cast<const __half2*>(&pk[q]), zero2, chk16);
+    }
     const bool upper = sym && j0 > row0;  // strictly above the diagonal for every row of the block
     const bool on_diag = j0 == row0;      // the block holds the diagonal elements i == j
 
@@ -237,12 +249,12 @@ __device__ void epilogue_tile(const GemmLaunch& p, const GemmJob& job, int tile_
     __syncwarp();
 #pragma unroll
     for (int q = 0; q < 4; ++q)
-      *reinterpret_cast<uint4*>(stage + sw64_h(lane, 8 * q)) =
-          make_uint4(pack_half2(v[8 * q + 0], v[8 * q + 1]), pack_half2(v[8 * q + 2], v[8 * q + 3]),
-                     pack_half2(v[8 * q + 4], v[8 * q + 5]), pack_half2(v[8 * q + 6], v[8 * q + 7]));
+      *reinterpret_cast<uint4*>(stage + sw64_h(lane, 8 * q)) = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
     if (upper) {
 #pragma unroll
-      for (int k = 0; k < 32; ++k) *reinterpret_cast<__half*>(stage + 2048 + sw64_h(k, lane)) = __float2half_rn(v[k]);
+      for (int k = 0; k < 32; ++k)
+        *reinterpret_cast<uint16_t*>(stage + 2048 + sw64_h(k, lane)) =
+            static_cast<uint16_t>((k & 1) ? (pk[k >> 1] >> 16) : pk[k >> 1]);
     }
     __syncwarp();
     if (sym && on_diag) {
@@ -281,6 +293,7 @@ __device__ void epilogue_tile(const GemmLaunch& p, const GemmJob& job, int tile_
       }
     }
   }
+  bad |= __hisnan(__low2half(chk16)) || __hisnan(__high2half(chk16)) || chk32 != chk32;
 }
 
 // ---------------------------------------------------------------------------- the kernel

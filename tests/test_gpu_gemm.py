@@ -115,3 +115,48 @@ def test_deterministic(dm):
     dm.gemm_f16(xd, xd, d2, symmetric=True)
     dm.check_status()
     assert torch.equal(d1, d2)
+
+
+@pytest.mark.parametrize("sym", [False, True])
+@pytest.mark.parametrize("m,k", [(300, 520), (512, 256)])
+def test_overflow_reported(dm, m, k, sym):
+    """A result past the fp16 range raises the NONFINITE status: here only row and column m-1 of X Xᵀ
+    (the ragged last tile when m = 300; in the mirrored part when symmetric) exceed 65504."""
+    rng = np.random.default_rng(m + k)
+    x, xd = _half(rng, m, k, 1.0 / np.sqrt(k))
+    xd[m - 1, :] = 64.0  # D[m-1][m-1] = 4096 k > 65504
+    d = _out(m, m)
+    dm.gemm_f16(xd, xd, d, b_trans=True, symmetric=sym)
+    with pytest.raises(dm.DmuonError) as ei:
+        dm.check_status()
+    assert ei.value.status == dm.ERR_NONFINITE
+    dm.check_status()  # the word was cleared
+
+
+@pytest.mark.parametrize("b_trans", [True, False])
+def test_nan_reported(dm, b_trans):
+    """A NaN operand element propagates into its output row and is reported."""
+    rng = np.random.default_rng(21)
+    m, n, k = 260, 300, 264
+    a, ad = _half(rng, m, k, 1.0 / np.sqrt(k))
+    b, bd = _half(rng, n, k, 1.0) if b_trans else _half(rng, k, n, 1.0)
+    ad[137, 5] = float("nan")
+    d = _out(m, n)
+    dm.gemm_f16(ad, bd, d, b_trans=b_trans)
+    with pytest.raises(dm.DmuonError) as ei:
+        dm.check_status()
+    assert ei.value.status == dm.ERR_NONFINITE
+    dm.check_status()
+
+
+def test_large_finite_not_reported(dm):
+    """Results just inside the fp16 range (up to 65504 after rounding) are not flagged."""
+    m, k = 256, 64
+    xd = torch.full((m, k), 32.0, dtype=torch.float16, device="cuda")  # every element of X Xᵀ: 65536 k / 64
+    xd[:, 63] = 0.0
+    xd[:, 62] = 31.0  # row sums of squares: 62 * 1024 + 961 = 64449
+    d = _out(m, m)
+    dm.gemm_f16(xd, xd, d, b_trans=True, symmetric=True)
+    dm.check_status()
+    got = d.float().cpu().numpy()
+    assert np.all(got == 64448.0)  # 64449 rounds to the fp16 neighbour 64448
