@@ -46,6 +46,7 @@ struct Cfg {
   static constexpr int kBarrierBytes = 256;
   static constexpr int kSmemBytes = kStages * kStageBytes + kEpiBytes + kBarrierBytes + 1024;  // + alignment slack
   static_assert(kStageBytes % 1024 == 0, "stages must keep 1024-byte alignment for 128B swizzle");
+  static_assert(kStages >= 3, "the MMA issuer checks three ring slots at a time");
   static_assert((2 * kStages + 5) * 8 + 8 <= kBarrierBytes, "barrier area too small");
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
@@ -424,9 +425,25 @@ __device__ __forceinline__ void gemm_tc_body(const GemmLaunch& p) {
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
         const uint32_t idesc = instr_desc<C::kTileM, BN>(bmn);
         for (int kb = 0; kb < nkb; ++kb) {
-          if (!wait_fast(&full[stage], phase, abort_flag, p.status)) {
-            ok = false;
-            break;
+          // Full barriers are checked three ring slots at a time (this slot and the next two of the tile):
+          // the probes overlap one another, and the MMA issue is interrupted by a barrier check once per
+          // twelve MMAs instead of once per four.
+          if (kb % 3 == 0) {
+            const int s1 = stage + 1 == C::kStages ? 0 : stage + 1;
+            const uint32_t p1 = stage + 1 == C::kStages ? phase ^ 1u : phase;
+            const int s2 = s1 + 1 == C::kStages ? 0 : s1 + 1;
+            const uint32_t p2 = s1 + 1 == C::kStages ? p1 ^ 1u : p1;
+            const bool r0 = mbar_try_wait(&full[stage], phase);
+            const bool r1 = kb + 1 >= nkb || mbar_try_wait(&full[s1], p1);
+            const bool r2 = kb + 2 >= nkb || mbar_try_wait(&full[s2], p2);
+            if (!(r0 && r1 && r2)) {
+              if ((!r0 && !wait_bounded(&full[stage], phase, abort_flag, p.status, kWaitLimitNs, true)) ||
+                  (!r1 && !wait_bounded(&full[s1], p1, abort_flag, p.status, kWaitLimitNs, true)) ||
+                  (!r2 && !wait_bounded(&full[s2], p2, abort_flag, p.status, kWaitLimitNs, true))) {
+                ok = false;
+                break;
+              }
+            }
           }
           tc_fence_after();
           const uint32_t sa = smem_u32(smem + stage * C::kStageBytes);
