@@ -91,7 +91,8 @@ def total_flops(shapes, backend, restarts=(2,)):
 
 
 # The GEMM's DRAM traffic depends on the kernel and on the planner's tile order.
-GEMM_SOURCES = [os.path.join(ROOT, "newton_schulz_momentum_gb300", "csrc", f) for f in ("gemm_tc.cu", "api.cu")]
+GEMM_SOURCES = [os.path.join(ROOT, "newton_schulz_momentum_gb300", "csrc", f)
+                for f in ("gemm_tc.cu", "tc_ptx.h", "internal.h", "api.cu")]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gemm_tc_dram_traffic.json")
 
 
