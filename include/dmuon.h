@@ -131,6 +131,35 @@ DMUON_API int dmuon_muon_step(int count, float* const* params, const void* const
                     const int* restarts, int n_restarts, int backend, float eps, void* cuda_stream);
 
 /*
+ * dmuon_muon_step_host -- dmuon_muon_step with the step's gradients arriving from host memory, the form a
+ * caller whose gradients are produced or staged on the host uses. (The pages transfer gradients between
+ * ranks, not from the host; this is the single-GPU form of "gradients in, update out".) Equivalent to
+ * copying every grads_host[i] into grads[i] and then calling dmuon_muon_step, with identical results,
+ * but the copies overlap the computation: the matrices are taken in `groups` consecutive groups of about
+ * equal gradient bytes; group g's copies run on the library's copy stream while earlier groups compute on
+ * cuda_stream, and group g's momentum pass waits only for its own copies. Each group runs its row-wise
+ * passes and Newton-Schulz phases as grouped launches of its own.
+ *
+ *   grads_host  host array of `count` host pointers to the gradients (rows[i] x cols[i], `grad_dtype`,
+ *               row-major, contiguous). For the copies to overlap they must be page-locked
+ *               (cudaHostAlloc / cudaHostRegister); pageable memory gives the same results without the
+ *               overlap. The caller keeps them unchanged until cuda_stream has passed this call.
+ *   grads       host array of `count` device buffers (as in dmuon_muon_step) receiving the gradients;
+ *               they are overwritten.
+ *   groups      pipeline depth in [1, 64]; <= 0 lets the library choose (one group per ~3 GiB of
+ *               gradients, at most 8). More groups than matrices gives one matrix per group.
+ *   Other arguments as in dmuon_muon_step.
+ * Ordering: the copies start after all work enqueued on cuda_stream before the call and after the
+ * previous dmuon_muon_step_host call on this device has read its gradients; all of the call's work,
+ * copies included, is complete when cuda_stream reaches the point after it. Not graph-capturable.
+ */
+DMUON_API int dmuon_muon_step_host(int count, float* const* params, const void* const* grads_host, void* const* grads,
+                                   int grad_dtype, float* const* momenta, const int64_t* rows, const int64_t* cols,
+                                   float* norms_out, float lr, float beta, const float* coeffs, int steps,
+                                   const int* restarts, int n_restarts, int backend, float eps, int groups,
+                                   void* cuda_stream);
+
+/*
  * dmuon_momentum_normalize -- the first half of dmuon_muon_step on its own ("精度流水线", stage 1,
  * preceded by the momentum accumulate): for each matrix
  *   M_i <- beta * M_i + G_i (skipped when grads == NULL: M_i is then only read),

@@ -44,7 +44,7 @@ EXPORTS = (
     "dmuon_ns", "dmuon_muon_step", "dmuon_momentum_normalize", "dmuon_gemm_f16", "dmuon_check_status",
     "dmuon_last_error", "dmuon_version", "dmuon_set_workspace_limit", "dmuon_workspace_size",
     "dmuon_release_workspace", "dmuon_timing_enable", "dmuon_timing_read", "dmuon_momentum_normalize_noalloc",
-    "dmuon_assign_owners", "dmuon_adamw_step", "dmuon_ns_tp",
+    "dmuon_assign_owners", "dmuon_adamw_step", "dmuon_ns_tp", "dmuon_muon_step_host",
 )
 COST_MODELS = {"elements": 0, "gram_flops": 1, "direct_flops": 2}
 NOALLOC_MAX_ELEMS = 268435456
@@ -82,6 +82,8 @@ def lib():
     L.dmuon_ns_tp.argtypes = [vp, i64, i64, i32, _c_fp, i32, _c_ip, i32, f32, vp]
     L.dmuon_muon_step.argtypes = [i32, _c_vpp, _c_vpp, i32, _c_vpp, _c_i64p, _c_i64p, vp, f32, f32, _c_fp, i32,
                                   _c_ip, i32, i32, f32, vp]
+    L.dmuon_muon_step_host.argtypes = [i32, _c_vpp, _c_vpp, _c_vpp, i32, _c_vpp, _c_i64p, _c_i64p, vp, f32, f32,
+                                       _c_fp, i32, _c_ip, i32, i32, f32, i32, vp]
     L.dmuon_momentum_normalize.argtypes = [i32, _c_vpp, i32, _c_vpp, _c_i64p, _c_i64p, _c_vpp, vp, f32, f32, vp]
     L.dmuon_gemm_f16.argtypes = [i64, i64, i64, vp, i64, vp, i64, i32, vp, i64, vp, i64, f32, f32, f32, i32, vp]
     L.dmuon_check_status.argtypes = [vp]
@@ -211,10 +213,14 @@ class MuonStep:
 
         step = MuonStep(params, grads, momenta, coeffs=POLAR_EXPRESS, restarts=(2,), backend="gram")
         step(lr=0.02, beta=0.95)          # enqueued on the current CUDA stream
+
+    With host_grads (CPU tensors shaped like grads, ideally pinned) each call is one
+    dmuon_muon_step_host: the gradients are copied from host_grads into grads inside the call, in
+    `groups` pipelined groups (0: the library chooses) whose copies overlap the computation.
     """
 
     def __init__(self, params, grads, momenta, coeffs=POLAR_EXPRESS, restarts=DEFAULT_RESTARTS, backend="gram",
-                 eps=1e-7, norms_out=None):
+                 eps=1e-7, norms_out=None, host_grads=None, groups=0):
         n = len(params)
         if not (len(grads) == len(momenta) == n) or n == 0:
             raise ValueError("params, grads and momenta must be non-empty lists of equal length")
@@ -236,8 +242,24 @@ class MuonStep:
         self._backend = _backend(backend)
         self._eps = float(eps)
         self._norms = _ptr(norms_out)
+        self._H = None
+        if host_grads is not None:
+            if len(host_grads) != n:
+                raise ValueError("host_grads must have one tensor per matrix")
+            for h, g in zip(host_grads, grads):
+                if h.shape != g.shape or h.dtype != g.dtype or not h.is_contiguous() or h.is_cuda:
+                    raise ValueError("each host gradient must be a contiguous CPU tensor shaped and typed like its grad")
+            self._keep = self._keep + (list(host_grads),)
+            self._H = (ctypes.c_void_p * n)(*[t.data_ptr() for t in host_grads])
+            self._groups = int(groups)
 
     def __call__(self, lr=0.02, beta=0.95, stream=None):
+        if self._H is not None:
+            _check(lib().dmuon_muon_step_host(self._n, self._P, self._H, self._G, self._gdtype, self._M, self._rows,
+                                              self._cols, self._norms, float(lr), float(beta), self._coeffs,
+                                              self._steps, self._restarts, self._nr, self._backend, self._eps,
+                                              self._groups, _stream(stream)))
+            return
         _check(lib().dmuon_muon_step(self._n, self._P, self._G, self._gdtype, self._M, self._rows, self._cols,
                                      self._norms, float(lr), float(beta), self._coeffs, self._steps, self._restarts,
                                      self._nr, self._backend, self._eps, _stream(stream)))

@@ -54,6 +54,7 @@ int cuda_fail(cudaError_t e, const char* what) {
 
 constexpr size_t kNone = ~size_t(0);
 constexpr int64_t kMaxDim = int64_t(1) << 24;
+constexpr int kMaxGroups = 64;  // pipeline groups of one dmuon_muon_step_host call
 
 int64_t round_up(int64_t v, int64_t a) { return (v + a - 1) / a * a; }
 
@@ -66,12 +67,13 @@ constexpr int kJobTpReduce = 1 << 10;
 struct PlanKey {
   int kind = -1, backend = 0, steps = 0, gdtype = 0;
   int shards = 0;  // kPlanNsTp: column shards along the long side
+  int groups = 1;  // kPlanMuon: consecutive matrix groups run one after another (host-gradient pipeline)
   std::vector<int> restarts;
   std::vector<int64_t> rows, cols;
   std::vector<uintptr_t> ptrs;  // W, G, M, X_out per matrix
   bool operator==(const PlanKey& o) const {
     return kind == o.kind && backend == o.backend && steps == o.steps && gdtype == o.gdtype && shards == o.shards &&
-           restarts == o.restarts && rows == o.rows && cols == o.cols && ptrs == o.ptrs;
+           groups == o.groups && restarts == o.restarts && rows == o.rows && cols == o.cols && ptrs == o.ptrs;
   }
 };
 
@@ -102,6 +104,7 @@ struct JobSpec {
 
 struct LaunchRec {
   int first_job, njobs, first_tile, ntiles, tile, coef;
+  int group = 0;  // the matrix group whose phases this launch runs
   int tp_reduce = 0;  // 1: not a GEMM but the reduction of per-shard Gram partials (tp_mat's)
   int tp_mat = 0;
 };
@@ -112,6 +115,11 @@ struct Plan {
   std::vector<MatInfo> mats;
   std::vector<std::vector<JobSpec>> phases;  // one grouped launch each
   std::vector<int> phase_coef;
+  std::vector<int> phase_group;
+  // Matrix groups [group_begin[g], group_begin[g + 1]): each runs its row-wise passes and then all its
+  // Newton-Schulz phases before the next group starts. One group unless a host-gradient call pipelines
+  // its copies against the computation.
+  std::vector<int> group_begin;
   int64_t nchunks = 0, ncast = 0;
   size_t off_rowmats = 0, off_chunk = 0, off_tilep = 0, off_partials = 0, off_norms = 0, off_inv = 0;
   size_t off_jobs = 0, off_tiles = 0, bytes = 0;
@@ -161,6 +169,11 @@ struct DeviceState {
   size_t arena_bytes = 0;
   Plan plan;
   AdamPlan adam;
+  // Host-gradient pipeline (dmuon_muon_step_host): the copy stream, an event marking the caller's stream
+  // at entry, and per group the "gradients arrived" and "gradients read by the momentum pass" events.
+  cudaStream_t copy_stream = nullptr;
+  cudaEvent_t entry = nullptr;
+  std::vector<cudaEvent_t> copied, read;
 };
 
 std::mutex g_mu;
@@ -557,28 +570,47 @@ int build_plan_host(Plan& pl, const PlanKey& key, const std::vector<const void*>
                                          : static_cast<int>(pl.chunk_prefix[i + 1] - pl.chunk_prefix[i]);
     part += r.part_count;
   }
+  // Matrix groups: consecutive runs of about equal gradient bytes (one group for every other plan).
+  {
+    const int ng = (key.kind == kPlanMuon && !pl.small_fused) ? std::max(1, std::min(key.groups, nm)) : 1;
+    pl.group_begin.assign(1, 0);
+    int64_t total = 0;
+    for (int i = 0; i < nm; ++i) total += pl.mats[i].rows * pl.mats[i].cols;
+    int64_t run = 0;
+    for (int i = 0; i < nm && static_cast<int>(pl.group_begin.size()) < ng; ++i) {
+      run += pl.mats[i].rows * pl.mats[i].cols;
+      const int g = static_cast<int>(pl.group_begin.size());  // boundary being placed
+      // Close group g - 1 after matrix i once it holds its share, leaving a matrix for each later group.
+      if (run * ng >= total * g && nm - (i + 1) >= ng - g) pl.group_begin.push_back(i + 1);
+    }
+    pl.group_begin.push_back(nm);
+  }
   if (pl.small_fused) {
     pl.off_small = lay.take(sizeof(SmallJob) * nm, 256);
   } else if (key.kind != kPlanMomNorm) {
-    std::vector<int> idx_gram, idx_direct;
-    for (int i = 0; i < nm; ++i) (pl.mats[i].direct ? idx_direct : idx_gram).push_back(i);
-    std::vector<std::vector<JobSpec>> gp, dp;
-    std::vector<int> gc, dc;
-    if (!idx_gram.empty()) build_gram_phases(pl, key.restarts, key.steps, idx_gram, gp, gc);
-    if (!idx_direct.empty()) build_direct_phases(pl, key.steps, idx_direct, dp, dc);
-    // Both sequences advance step by step; the t-th launch of step k carries the t-th phase of step k of
-    // each (their matrices are disjoint, and each sequence keeps its own order).
-    size_t gi = 0, di = 0;
-    for (int k = 0; k < key.steps; ++k) {
-      std::vector<std::vector<JobSpec>> ga, da;
-      while (gi < gp.size() && gc[gi] == k) ga.push_back(std::move(gp[gi++]));
-      while (di < dp.size() && dc[di] == k) da.push_back(std::move(dp[di++]));
-      for (size_t t = 0; t < std::max(ga.size(), da.size()); ++t) {
-        std::vector<JobSpec> ph;
-        if (t < ga.size()) ph.insert(ph.end(), ga[t].begin(), ga[t].end());
-        if (t < da.size()) ph.insert(ph.end(), da[t].begin(), da[t].end());
-        pl.phases.push_back(std::move(ph));
-        pl.phase_coef.push_back(k);
+    for (size_t g = 0; g + 1 < pl.group_begin.size(); ++g) {
+      std::vector<int> idx_gram, idx_direct;
+      for (int i = pl.group_begin[g]; i < pl.group_begin[g + 1]; ++i)
+        (pl.mats[i].direct ? idx_direct : idx_gram).push_back(i);
+      std::vector<std::vector<JobSpec>> gp, dp;
+      std::vector<int> gc, dc;
+      if (!idx_gram.empty()) build_gram_phases(pl, key.restarts, key.steps, idx_gram, gp, gc);
+      if (!idx_direct.empty()) build_direct_phases(pl, key.steps, idx_direct, dp, dc);
+      // Both sequences advance step by step; the t-th launch of step k carries the t-th phase of step k
+      // of each (their matrices are disjoint, and each sequence keeps its own order).
+      size_t gi = 0, di = 0;
+      for (int k = 0; k < key.steps; ++k) {
+        std::vector<std::vector<JobSpec>> ga, da;
+        while (gi < gp.size() && gc[gi] == k) ga.push_back(std::move(gp[gi++]));
+        while (di < dp.size() && dc[di] == k) da.push_back(std::move(dp[di++]));
+        for (size_t t = 0; t < std::max(ga.size(), da.size()); ++t) {
+          std::vector<JobSpec> ph;
+          if (t < ga.size()) ph.insert(ph.end(), ga[t].begin(), ga[t].end());
+          if (t < da.size()) ph.insert(ph.end(), da[t].begin(), da[t].end());
+          pl.phases.push_back(std::move(ph));
+          pl.phase_coef.push_back(k);
+          pl.phase_group.push_back(static_cast<int>(g));
+        }
       }
     }
   }
@@ -595,6 +627,7 @@ int build_plan_host(Plan& pl, const PlanKey& key, const std::vector<const void*>
     L.njobs = static_cast<int>(ph.size());
     L.tile = launch_tile(ph);
     L.coef = pl.phase_coef[p];
+    L.group = pl.phase_group[p];
     L.first_tile = static_cast<int>(pl.tiles.size());
     if (!ph.empty() && (ph[0].flags & kJobTpReduce)) {
       L.tp_reduce = 1;
@@ -711,8 +744,12 @@ int bind_plan(DeviceState& ds, Plan& pl, cudaStream_t stream) {
   return DMUON_OK;
 }
 
+// Enqueue one run of a bound plan on `stream`. Groups run one after another, each its row-wise passes and
+// then its Newton-Schulz launches. With `group_ready` the stream first waits for event g before group g
+// (its gradients have arrived); with `group_read` event g is recorded once group g's momentum pass has
+// read its gradients.
 int run_plan(DeviceState& ds, const Plan& pl, const float* coeffs, float lr, float beta, float eps, float* norms_out,
-             cudaStream_t stream) {
+             cudaStream_t stream, const cudaEvent_t* group_ready = nullptr, const cudaEvent_t* group_read = nullptr) {
   char* base = ds.arena;
   RowLaunch rl;
   rl.mats = reinterpret_cast<const RowMat*>(base + pl.off_rowmats);
@@ -725,75 +762,111 @@ int run_plan(DeviceState& ds, const Plan& pl, const float* coeffs, float lr, flo
   rl.norms_out = norms_out;
   rl.beta = beta;
   rl.eps = eps;
-  if (pl.key.kind == kPlanNsTp) {
-    // One sum of squares per shard and row slab; their fixed-order sum is the one scalar all-reduce.
-    const MatInfo& mi = pl.mats[0];
-    ShardSumsqLaunch sl;
-    std::memset(&sl, 0, sizeof(sl));
-    sl.x = mi.M;
-    sl.rows = mi.rows;
-    sl.cols = mi.cols;
-    sl.trans = mi.trans ? 1 : 0;
-    sl.shards = pl.key.shards;
-    sl.slabs = pl.tp_slabs;
-    for (int t = 0; t <= pl.key.shards; ++t) sl.bounds[t] = pl.shard_bounds[t];
-    sl.partials = rl.partials;
-    DM_CUDA(timed(0, stream, [&] { return launch_shard_sumsq(sl, stream); }), "shard sum-of-squares launch");
-  } else {
-    DM_CUDA(timed(0, stream, [&] { return launch_momentum_sumsq(rl, pl.nchunks, stream); }),
-            "momentum/sum-of-squares launch");
-  }
-  DM_CUDA(timed(1, stream, [&] { return launch_finalize_norms(rl, stream); }), "norm launch");
-  DM_CUDA(timed(2, stream, [&] { return launch_normalize_cast(rl, pl.ncast, stream); }), "normalise/cast launch");
-  if (pl.small_fused) {
-    SmallLaunch sl;
-    std::memset(&sl, 0, sizeof(sl));
-    sl.jobs = reinterpret_cast<const SmallJob*>(base + pl.off_small);
-    sl.njobs = static_cast<int>(pl.mats.size());
-    sl.steps = pl.key.steps;
-    sl.restart_mask = pl.restart_mask;
-    for (int k = 0; k < 3 * pl.key.steps; ++k) sl.coef[k] = coeffs[k];
-    sl.w_alpha = pl.key.kind == kPlanNs ? 0.f : 1.f;
-    sl.w_beta = pl.key.kind == kPlanNs ? 1.f : -lr;
-    sl.status = ds.status;
-    DM_CUDA(timed(3, stream, [&] { return launch_ns_small(sl, ds.sms, stream); }), "small-matrix kernel launch");
-    return DMUON_OK;
-  }
   const GemmJob* jobs = reinterpret_cast<const GemmJob*>(base + pl.off_jobs);
   const GemmTile* tiles = reinterpret_cast<const GemmTile*>(base + pl.off_tiles);
   const bool overwrite = pl.key.kind == kPlanNs || pl.key.kind == kPlanNsTp;  // W = O, not W -= lr O
-  for (const LaunchRec& L : pl.launches) {
-    if (L.tp_reduce) {
-      const MatInfo& mi = pl.mats[L.tp_mat];
-      TpReduceLaunch tr;
-      tr.P = reinterpret_cast<const float*>(base + mi.P);
-      tr.shards = pl.key.shards;
-      tr.m = mi.m;
-      tr.ldp = mi.ldp;
-      tr.plane = mi.m * mi.ldp;
-      tr.R = reinterpret_cast<__half*>(base + mi.R);
-      tr.ldr = mi.ldm;
-      DM_CUDA(timed(5, stream, [&] { return launch_tp_reduce(tr, stream); }), "shard Gram reduction launch");
-      continue;
+  size_t li = 0;
+  const int ngroups = static_cast<int>(pl.group_begin.size()) - 1;
+  for (int g = 0; g < ngroups; ++g) {
+    const int i0 = pl.group_begin[g], i1 = pl.group_begin[g + 1];
+    if (group_ready) DM_CUDA(cudaStreamWaitEvent(stream, group_ready[g], 0), "wait for a group's gradients");
+    RowLaunch rg = rl;
+    rg.mats += i0;
+    rg.nmats = i1 - i0;
+    rg.chunk_prefix += i0;
+    rg.tile_prefix += i0;
+    rg.norms += i0;
+    rg.inv += i0;
+    if (rg.norms_out) rg.norms_out += i0;
+    rg.chunk_base = pl.chunk_prefix[i0];
+    rg.tile_base = pl.tile_prefix[i0];
+    const int64_t nchunks = pl.chunk_prefix[i1] - pl.chunk_prefix[i0];
+    const int64_t ncast = pl.tile_prefix[i1] - pl.tile_prefix[i0];
+    if (pl.key.kind == kPlanNsTp) {
+      // One sum of squares per shard and row slab; their fixed-order sum is the one scalar all-reduce.
+      const MatInfo& mi = pl.mats[0];
+      ShardSumsqLaunch sl;
+      std::memset(&sl, 0, sizeof(sl));
+      sl.x = mi.M;
+      sl.rows = mi.rows;
+      sl.cols = mi.cols;
+      sl.trans = mi.trans ? 1 : 0;
+      sl.shards = pl.key.shards;
+      sl.slabs = pl.tp_slabs;
+      for (int t = 0; t <= pl.key.shards; ++t) sl.bounds[t] = pl.shard_bounds[t];
+      sl.partials = rl.partials;
+      DM_CUDA(timed(0, stream, [&] { return launch_shard_sumsq(sl, stream); }), "shard sum-of-squares launch");
+    } else {
+      DM_CUDA(timed(0, stream, [&] { return launch_momentum_sumsq(rg, nchunks, stream); }),
+              "momentum/sum-of-squares launch");
     }
-    GemmLaunch gl;
-    std::memset(&gl, 0, sizeof(gl));
-    gl.jobs = jobs + L.first_job;
-    gl.tiles = tiles + L.first_tile;
-    gl.ntiles = L.ntiles;
-    gl.a = coeffs[3 * L.coef + 0];
-    gl.b = coeffs[3 * L.coef + 1];
-    gl.c = coeffs[3 * L.coef + 2];
-    gl.w_alpha = overwrite ? 0.f : 1.f;
-    gl.w_beta = overwrite ? 1.f : -lr;
-    gl.status = ds.status;
-    const int units = std::min(L.ntiles, gemm_max_units(L.tile, ds.sms));
-    DM_CUDA(timed(3, stream, [&] { return launch_gemm(gl, L.tile, units, stream); }), "tensor-core GEMM launch");
+    if (group_read) DM_CUDA(cudaEventRecord(group_read[g], stream), "record a group's gradients as read");
+    DM_CUDA(timed(1, stream, [&] { return launch_finalize_norms(rg, stream); }), "norm launch");
+    DM_CUDA(timed(2, stream, [&] { return launch_normalize_cast(rg, ncast, stream); }), "normalise/cast launch");
+    if (pl.small_fused) {
+      SmallLaunch sl;
+      std::memset(&sl, 0, sizeof(sl));
+      sl.jobs = reinterpret_cast<const SmallJob*>(base + pl.off_small);
+      sl.njobs = static_cast<int>(pl.mats.size());
+      sl.steps = pl.key.steps;
+      sl.restart_mask = pl.restart_mask;
+      for (int k = 0; k < 3 * pl.key.steps; ++k) sl.coef[k] = coeffs[k];
+      sl.w_alpha = pl.key.kind == kPlanNs ? 0.f : 1.f;
+      sl.w_beta = pl.key.kind == kPlanNs ? 1.f : -lr;
+      sl.status = ds.status;
+      DM_CUDA(timed(3, stream, [&] { return launch_ns_small(sl, ds.sms, stream); }), "small-matrix kernel launch");
+      continue;  // a fused plan has one group
+    }
+    for (; li < pl.launches.size() && pl.launches[li].group == g; ++li) {
+      const LaunchRec& L = pl.launches[li];
+      if (L.tp_reduce) {
+        const MatInfo& mi = pl.mats[L.tp_mat];
+        TpReduceLaunch tr;
+        tr.P = reinterpret_cast<const float*>(base + mi.P);
+        tr.shards = pl.key.shards;
+        tr.m = mi.m;
+        tr.ldp = mi.ldp;
+        tr.plane = mi.m * mi.ldp;
+        tr.R = reinterpret_cast<__half*>(base + mi.R);
+        tr.ldr = mi.ldm;
+        DM_CUDA(timed(5, stream, [&] { return launch_tp_reduce(tr, stream); }), "shard Gram reduction launch");
+        continue;
+      }
+      GemmLaunch gl;
+      std::memset(&gl, 0, sizeof(gl));
+      gl.jobs = jobs + L.first_job;
+      gl.tiles = tiles + L.first_tile;
+      gl.ntiles = L.ntiles;
+      gl.a = coeffs[3 * L.coef + 0];
+      gl.b = coeffs[3 * L.coef + 1];
+      gl.c = coeffs[3 * L.coef + 2];
+      gl.w_alpha = overwrite ? 0.f : 1.f;
+      gl.w_beta = overwrite ? 1.f : -lr;
+      gl.status = ds.status;
+      const int units = std::min(L.ntiles, gemm_max_units(L.tile, ds.sms));
+      DM_CUDA(timed(3, stream, [&] { return launch_gemm(gl, L.tile, units, stream); }), "tensor-core GEMM launch");
+    }
   }
   return DMUON_OK;
 }
 
-// Shared body of the three plan-based entry points.
+// Make the device's cached plan the one for `key`, building and binding it if it is not. Caller holds g_mu.
+// *rebuilt tells whether it had to be built.
+int ensure_plan(DeviceState& ds, const PlanKey& key, const std::vector<const void*>& G, const std::vector<float*>& Mom,
+                const std::vector<float*>& W, const std::vector<void*>& xout, cudaStream_t stream,
+                bool* rebuilt = nullptr) {
+  if (rebuilt) *rebuilt = false;
+  if (ds.plan.bound && ds.plan.key == key) return DMUON_OK;
+  if (rebuilt) *rebuilt = true;
+  ds.plan = Plan();
+  int st = build_plan_host(ds.plan, key, G, Mom, W, xout);
+  if (st != DMUON_OK) return st;
+  st = bind_plan(ds, ds.plan, stream);
+  if (st != DMUON_OK) ds.plan = Plan();
+  return st;
+}
+
+// Shared body of the plan-based entry points that take device buffers.
 int plan_and_run(const PlanKey& key, const std::vector<const void*>& G, const std::vector<float*>& Mom,
                  const std::vector<float*>& W, const std::vector<void*>& xout, const float* coeffs, float lr,
                  float beta, float eps, float* norms_out, cudaStream_t stream) {
@@ -801,17 +874,68 @@ int plan_and_run(const PlanKey& key, const std::vector<const void*>& G, const st
   DeviceState* ds = nullptr;
   int st = current_device(&ds);
   if (st != DMUON_OK) return st;
-  if (!(ds->plan.bound && ds->plan.key == key)) {
-    ds->plan = Plan();
-    st = build_plan_host(ds->plan, key, G, Mom, W, xout);
-    if (st != DMUON_OK) return st;
-    st = bind_plan(*ds, ds->plan, stream);
-    if (st != DMUON_OK) {
-      ds->plan = Plan();
-      return st;
-    }
-  }
+  st = ensure_plan(*ds, key, G, Mom, W, xout, stream);
+  if (st != DMUON_OK) return st;
   return run_plan(*ds, ds->plan, coeffs, lr, beta, eps, norms_out, stream);
+}
+
+// The copy stream and at least `n` pairs of group events of the host-gradient pipeline.
+int ensure_pipeline(DeviceState& ds, size_t n) {
+  if (!ds.copy_stream) DM_CUDA(cudaStreamCreateWithFlags(&ds.copy_stream, cudaStreamNonBlocking), "create copy stream");
+  if (!ds.entry) DM_CUDA(cudaEventCreateWithFlags(&ds.entry, cudaEventDisableTiming), "create event");
+  while (ds.copied.size() < n) {
+    cudaEvent_t a = nullptr, b = nullptr;
+    DM_CUDA(cudaEventCreateWithFlags(&a, cudaEventDisableTiming), "create event");
+    if (cudaEventCreateWithFlags(&b, cudaEventDisableTiming) != cudaSuccess) {
+      cudaEventDestroy(a);
+      return fail(DMUON_ERR_CUDA, "create event failed");
+    }
+    ds.copied.push_back(a);
+    ds.read.push_back(b);
+  }
+  return DMUON_OK;
+}
+
+int check_matrix_list(int count, const int64_t* rows, const int64_t* cols);
+
+// Validation and key of dmuon_muon_step (shared with dmuon_muon_step_host).
+int muon_key(int count, float* const* params, const void* const* grads, int grad_dtype, float* const* momenta,
+             const int64_t* rows, const int64_t* cols, float* norms_out, float lr, float beta, const float* coeffs,
+             int steps, const int* restarts, int n_restarts, int backend, float eps, PlanKey& key,
+             std::vector<const void*>& G, std::vector<float*>& Mo, std::vector<float*>& W) {
+  int st = check_matrix_list(count, rows, cols);
+  if (st != DMUON_OK) return st;
+  if (!params || !grads || !momenta) return fail(DMUON_ERR_INVALID_ARG, "params/grads/momenta arrays are NULL");
+  if (grad_dtype != DMUON_F32 && grad_dtype != DMUON_BF16)
+    return fail(DMUON_ERR_INVALID_ARG, "grad_dtype must be DMUON_F32 (0) or DMUON_BF16 (1)");
+  if (!std::isfinite(lr) || !std::isfinite(beta)) return fail(DMUON_ERR_INVALID_ARG, "lr and beta must be finite");
+  if (norms_out && !aligned16(norms_out) && (reinterpret_cast<uintptr_t>(norms_out) & 3))
+    return fail(DMUON_ERR_INVALID_ARG, "norms_out must be 4-byte aligned");
+  st = check_ns_args(coeffs, steps, restarts, n_restarts, backend, eps);
+  if (st != DMUON_OK) return st;
+  key = PlanKey();
+  key.kind = kPlanMuon;
+  key.backend = backend;
+  key.steps = steps;
+  key.gdtype = grad_dtype;
+  if (backend != DMUON_NS_DIRECT) key.restarts.assign(restarts, restarts + n_restarts);
+  key.rows.assign(rows, rows + count);
+  key.cols.assign(cols, cols + count);
+  G.assign(count, nullptr);
+  Mo.assign(count, nullptr);
+  W.assign(count, nullptr);
+  for (int i = 0; i < count; ++i) {
+    if (!params[i] || !grads[i] || !momenta[i]) return fail(DMUON_ERR_INVALID_ARG, "matrix %d has a NULL pointer", i);
+    if (!aligned16(params[i]) || !aligned16(grads[i]) || !aligned16(momenta[i]))
+      return fail(DMUON_ERR_INVALID_ARG, "matrix %d: device buffers must be 16-byte aligned", i);
+    G[i] = grads[i];
+    Mo[i] = momenta[i];
+    W[i] = params[i];
+    key.ptrs.push_back(reinterpret_cast<uintptr_t>(params[i]));
+    key.ptrs.push_back(reinterpret_cast<uintptr_t>(grads[i]));
+    key.ptrs.push_back(reinterpret_cast<uintptr_t>(momenta[i]));
+  }
+  return DMUON_OK;
 }
 
 int check_matrix_list(int count, const int64_t* rows, const int64_t* cols) {
@@ -895,40 +1019,74 @@ int dmuon_muon_step(int count, float* const* params, const void* const* grads, i
                     const float* coeffs, int steps, const int* restarts, int n_restarts, int backend, float eps,
                     void* cuda_stream) {
   try {
-    int st = check_matrix_list(count, rows, cols);
-    if (st != DMUON_OK) return st;
-    if (!params || !grads || !momenta) return fail(DMUON_ERR_INVALID_ARG, "params/grads/momenta arrays are NULL");
-    if (grad_dtype != DMUON_F32 && grad_dtype != DMUON_BF16)
-      return fail(DMUON_ERR_INVALID_ARG, "grad_dtype must be DMUON_F32 (0) or DMUON_BF16 (1)");
-    if (!std::isfinite(lr) || !std::isfinite(beta)) return fail(DMUON_ERR_INVALID_ARG, "lr and beta must be finite");
-    if (norms_out && !aligned16(norms_out) && (reinterpret_cast<uintptr_t>(norms_out) & 3))
-      return fail(DMUON_ERR_INVALID_ARG, "norms_out must be 4-byte aligned");
-    st = check_ns_args(coeffs, steps, restarts, n_restarts, backend, eps);
-    if (st != DMUON_OK) return st;
     PlanKey key;
-    key.kind = kPlanMuon;
-    key.backend = backend;
-    key.steps = steps;
-    key.gdtype = grad_dtype;
-    if (backend != DMUON_NS_DIRECT) key.restarts.assign(restarts, restarts + n_restarts);
-    key.rows.assign(rows, rows + count);
-    key.cols.assign(cols, cols + count);
-    std::vector<const void*> G(count);
-    std::vector<float*> Mo(count), W(count);
+    std::vector<const void*> G;
+    std::vector<float*> Mo, W;
+    const int st = muon_key(count, params, grads, grad_dtype, momenta, rows, cols, norms_out, lr, beta, coeffs, steps,
+                            restarts, n_restarts, backend, eps, key, G, Mo, W);
+    if (st != DMUON_OK) return st;
     std::vector<void*> xo(count, nullptr);
-    for (int i = 0; i < count; ++i) {
-      if (!params[i] || !grads[i] || !momenta[i])
-        return fail(DMUON_ERR_INVALID_ARG, "matrix %d has a NULL pointer", i);
-      if (!aligned16(params[i]) || !aligned16(grads[i]) || !aligned16(momenta[i]))
-        return fail(DMUON_ERR_INVALID_ARG, "matrix %d: device buffers must be 16-byte aligned", i);
-      G[i] = grads[i];
-      Mo[i] = momenta[i];
-      W[i] = params[i];
-      key.ptrs.push_back(reinterpret_cast<uintptr_t>(params[i]));
-      key.ptrs.push_back(reinterpret_cast<uintptr_t>(grads[i]));
-      key.ptrs.push_back(reinterpret_cast<uintptr_t>(momenta[i]));
-    }
     return plan_and_run(key, G, Mo, W, xo, coeffs, lr, beta, eps, norms_out, static_cast<cudaStream_t>(cuda_stream));
+  } catch (const std::exception& e) {
+    return fail(DMUON_ERR_OOM, "host exception: %s", e.what());
+  }
+}
+
+int dmuon_muon_step_host(int count, float* const* params, const void* const* grads_host, void* const* grads,
+                         int grad_dtype, float* const* momenta, const int64_t* rows, const int64_t* cols,
+                         float* norms_out, float lr, float beta, const float* coeffs, int steps, const int* restarts,
+                         int n_restarts, int backend, float eps, int groups, void* cuda_stream) {
+  try {
+    PlanKey key;
+    std::vector<const void*> G;
+    std::vector<float*> Mo, W;
+    int st = muon_key(count, params, reinterpret_cast<const void* const*>(grads), grad_dtype, momenta, rows, cols,
+                      norms_out, lr, beta, coeffs, steps, restarts, n_restarts, backend, eps, key, G, Mo, W);
+    if (st != DMUON_OK) return st;
+    if (!grads_host) return fail(DMUON_ERR_INVALID_ARG, "grads_host is NULL");
+    for (int i = 0; i < count; ++i)
+      if (!grads_host[i]) return fail(DMUON_ERR_INVALID_ARG, "matrix %d has a NULL host gradient", i);
+    if (groups > kMaxGroups) return fail(DMUON_ERR_INVALID_ARG, "groups must be at most %d", kMaxGroups);
+    const size_t esize = grad_dtype == DMUON_BF16 ? 2 : 4;
+    if (groups <= 0) {
+      // One group per ~3 GiB of gradients, at most 8: the first group's copy is the part left exposed,
+      // and every group adds one launch per phase.
+      int64_t bytes = 0;
+      for (int i = 0; i < count; ++i) bytes += rows[i] * cols[i] * static_cast<int64_t>(esize);
+      const int64_t per_group = int64_t(3) << 30;
+      groups = static_cast<int>(std::min<int64_t>(8, std::max<int64_t>(1, (bytes + per_group - 1) / per_group)));
+    }
+    key.groups = groups;
+    cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceState* ds = nullptr;
+    st = current_device(&ds);
+    if (st != DMUON_OK) return st;
+    const size_t prev_groups = ds->copied.size();
+    bool rebuilt = false;
+    std::vector<void*> xo(count, nullptr);
+    st = ensure_plan(*ds, key, G, Mo, W, xo, stream, &rebuilt);
+    if (st != DMUON_OK) return st;
+    const Plan& pl = ds->plan;
+    const size_t ng = pl.group_begin.size() - 1;
+    st = ensure_pipeline(*ds, ng);
+    if (st != DMUON_OK) return st;
+    // Copies follow everything already enqueued on the caller's stream, and each group's copy follows the
+    // previous call's momentum pass over the same buffers (every previous group when the grouping changed).
+    DM_CUDA(cudaEventRecord(ds->entry, stream), "record entry event");
+    DM_CUDA(cudaStreamWaitEvent(ds->copy_stream, ds->entry, 0), "order copies after the caller's stream");
+    if (rebuilt)
+      for (size_t g = 0; g < prev_groups; ++g)
+        DM_CUDA(cudaStreamWaitEvent(ds->copy_stream, ds->read[g], 0), "order copies after the previous call");
+    for (size_t g = 0; g < ng; ++g) {
+      DM_CUDA(cudaStreamWaitEvent(ds->copy_stream, ds->read[g], 0), "order copies after the previous call");
+      for (int i = pl.group_begin[g]; i < pl.group_begin[g + 1]; ++i)
+        DM_CUDA(cudaMemcpyAsync(grads[i], grads_host[i], static_cast<size_t>(rows[i] * cols[i]) * esize,
+                                cudaMemcpyHostToDevice, ds->copy_stream),
+                "gradient copy");
+      DM_CUDA(cudaEventRecord(ds->copied[g], ds->copy_stream), "record a group's copy");
+    }
+    return run_plan(*ds, pl, coeffs, lr, beta, eps, norms_out, stream, ds->copied.data(), ds->read.data());
   } catch (const std::exception& e) {
     return fail(DMUON_ERR_OOM, "host exception: %s", e.what());
   }

@@ -171,6 +171,10 @@ struct RowLaunch {
   float* inv;                   // one per matrix: 1 / (||M||_F + eps)
   float* norms_out;             // optional user copy of norms
   float beta, eps;
+  // A launch may cover a contiguous group of the plan's matrices: `mats`, both prefixes, `norms`,
+  // `inv` and `norms_out` then point at the group's first entry, and block b works on momentum chunk
+  // chunk_base + b (cast tile tile_base + b) of the plan-wide numbering. Zero for a whole-plan launch.
+  int64_t chunk_base = 0, tile_base = 0;
 };
 
 // ------------------------------------------------------------------------------------------------

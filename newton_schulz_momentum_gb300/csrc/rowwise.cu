@@ -61,7 +61,7 @@ __device__ __forceinline__ T block_sum(T v, T* scratch) {
 
 __global__ void __launch_bounds__(kThreads) momentum_sumsq_kernel(const RowLaunch p) {
   __shared__ float red[kThreads / 32];
-  const int64_t chunk = blockIdx.x;
+  const int64_t chunk = p.chunk_base + blockIdx.x;
   const int mi = find_matrix(p.chunk_prefix, p.nmats, chunk);
   const RowMat mt = p.mats[mi];
   const int64_t local = chunk - p.chunk_prefix[mi];
@@ -154,7 +154,7 @@ __device__ __forceinline__ void store_half4(__half* dst, float a, float b, float
 
 __global__ void __launch_bounds__(kThreads) normalize_cast_kernel(const RowLaunch p) {
   __shared__ float tile[kCastTile][kCastTile + 1];
-  const int64_t t = blockIdx.x;
+  const int64_t t = p.tile_base + blockIdx.x;
   const int mi = find_matrix(p.tile_prefix, p.nmats, t);
   const RowMat mt = p.mats[mi];
   const int64_t local = t - p.tile_prefix[mi];

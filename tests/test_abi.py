@@ -90,6 +90,20 @@ def test_invalid_arguments_rejected_without_device(L):
     assert rc == dm.ERR_INVALID_ARG and "grad_dtype" in msg
     rc, msg = _status(L, L.dmuon_muon_step(0, P, P, 0, P, rows, cols, None, 0.02, 0.95, c, 5, r, 1, 1, 1e-7, None))
     assert rc == dm.ERR_INVALID_ARG and "count" in msg
+    # host-gradient step: the host array, each host pointer and the group count are checked first
+    H = (ctypes.c_void_p * 1)(8192)
+    rc, msg = _status(L, L.dmuon_muon_step_host(1, P, None, P, 1, P, rows, cols, None, 0.02, 0.95, c, 5, r, 1, 1,
+                                                1e-7, 0, None))
+    assert rc == dm.ERR_INVALID_ARG and "grads_host" in msg
+    rc, msg = _status(L, L.dmuon_muon_step_host(1, P, (ctypes.c_void_p * 1)(None), P, 1, P, rows, cols, None, 0.02,
+                                                0.95, c, 5, r, 1, 1, 1e-7, 0, None))
+    assert rc == dm.ERR_INVALID_ARG and "host gradient" in msg
+    rc, msg = _status(L, L.dmuon_muon_step_host(1, P, H, P, 1, P, rows, cols, None, 0.02, 0.95, c, 5, r, 1, 1, 1e-7,
+                                                65, None))
+    assert rc == dm.ERR_INVALID_ARG and "groups" in msg
+    rc, msg = _status(L, L.dmuon_muon_step_host(1, P, H, P, 3, P, rows, cols, None, 0.02, 0.95, c, 5, r, 1, 1, 1e-7,
+                                                0, None))
+    assert rc == dm.ERR_INVALID_ARG and "grad_dtype" in msg
 
 
 def test_flop_counts_closed_form():
