@@ -169,10 +169,26 @@ __global__ void __launch_bounds__(kThreads) normalize_cast_kernel(const RowLaunc
   const int tx = threadIdx.x & 15;   // 4-column group within the tile
   const int ty = threadIdx.x >> 4;   // row within a 16-row pass
 
+  constexpr int kPasses = kCastTile / 16;
+  const int64_t c = c0 + tx * 4;
+  // Interior tiles (every row and column in range, 16-byte rows): all of a thread's loads are issued
+  // before any use, so each thread keeps kPasses 16-byte reads in flight.
+  const bool interior = vec_in && r0 + kCastTile <= mt.rows && c0 + kCastTile <= mt.cols;
+
   if (!mt.trans) {
-    for (int pass = 0; pass < kCastTile / 16; ++pass) {
+    if (interior && vec_out) {
+      float4 v[kPasses];
+#pragma unroll
+      for (int pass = 0; pass < kPasses; ++pass)
+        v[pass] = __ldcs(reinterpret_cast<const float4*>(mt.M + (r0 + pass * 16 + ty) * mt.cols + c));
+#pragma unroll
+      for (int pass = 0; pass < kPasses; ++pass)
+        store_half4(mt.X + (r0 + pass * 16 + ty) * mt.ldx + c, v[pass].x * inv, v[pass].y * inv, v[pass].z * inv,
+                    v[pass].w * inv);
+      return;
+    }
+    for (int pass = 0; pass < kPasses; ++pass) {
       const int64_t r = r0 + pass * 16 + ty;
-      const int64_t c = c0 + tx * 4;
       if (r >= mt.rows) continue;
       const float* src = mt.M + r * mt.cols + c;
       __half* dst = mt.X + r * mt.ldx + c;
@@ -188,21 +204,35 @@ __global__ void __launch_bounds__(kThreads) normalize_cast_kernel(const RowLaunc
   }
 
   // Tall matrix: X (cols x rows) = (M * inv)^T.
-  for (int pass = 0; pass < kCastTile / 16; ++pass) {
-    const int rr = pass * 16 + ty;
-    const int64_t r = r0 + rr;
-    const int64_t c = c0 + tx * 4;
-    if (r >= mt.rows) continue;
-    const float* src = mt.M + r * mt.cols + c;
-    if (vec_in && c + 4 <= mt.cols) {
-      const float4 v = *reinterpret_cast<const float4*>(src);
-      tile[rr][tx * 4 + 0] = v.x;
-      tile[rr][tx * 4 + 1] = v.y;
-      tile[rr][tx * 4 + 2] = v.z;
-      tile[rr][tx * 4 + 3] = v.w;
-    } else {
-      for (int k = 0; k < 4; ++k)
-        if (c + k < mt.cols) tile[rr][tx * 4 + k] = src[k];
+  if (interior) {
+    float4 v[kPasses];
+#pragma unroll
+    for (int pass = 0; pass < kPasses; ++pass)
+      v[pass] = __ldcs(reinterpret_cast<const float4*>(mt.M + (r0 + pass * 16 + ty) * mt.cols + c));
+#pragma unroll
+    for (int pass = 0; pass < kPasses; ++pass) {
+      const int rr = pass * 16 + ty;
+      tile[rr][tx * 4 + 0] = v[pass].x;
+      tile[rr][tx * 4 + 1] = v[pass].y;
+      tile[rr][tx * 4 + 2] = v[pass].z;
+      tile[rr][tx * 4 + 3] = v[pass].w;
+    }
+  } else {
+    for (int pass = 0; pass < kPasses; ++pass) {
+      const int rr = pass * 16 + ty;
+      const int64_t r = r0 + rr;
+      if (r >= mt.rows) continue;
+      const float* src = mt.M + r * mt.cols + c;
+      if (vec_in && c + 4 <= mt.cols) {
+        const float4 v = *reinterpret_cast<const float4*>(src);
+        tile[rr][tx * 4 + 0] = v.x;
+        tile[rr][tx * 4 + 1] = v.y;
+        tile[rr][tx * 4 + 2] = v.z;
+        tile[rr][tx * 4 + 3] = v.w;
+      } else {
+        for (int k = 0; k < 4; ++k)
+          if (c + k < mt.cols) tile[rr][tx * 4 + k] = src[k];
+      }
     }
   }
   __syncthreads();
