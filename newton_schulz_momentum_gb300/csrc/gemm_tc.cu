@@ -54,6 +54,11 @@ struct Cfg {
 // ---------------------------------------------------------------------------- tile bookkeeping
 
 constexpr int kSingleBand = 8;  // tile rows per raster band of a single-job launch
+// L2 priorities of the TMA traffic: operand loads that other tiles of the launch re-read are kept
+// (evict_last), epilogue stores and reduce-adds are streamed through (evict_first).
+constexpr bool kKeepA = true;
+constexpr bool kKeepB = true;
+constexpr bool kStreamOut = true;
 
 struct TileRef {
   const GemmJob* job;
@@ -107,9 +112,18 @@ __device__ __forceinline__ Scalars recipe_scalars(const GemmLaunch& p, int recip
 }
 
 
+__device__ __forceinline__ void store_out(const CUtensorMap* map, uint32_t src, int c0, int c1, uint64_t pol) {
+  if constexpr (kStreamOut) tma_store_2d_hint(map, src, c0, c1, pol);
+  else tma_store_2d(map, src, c0, c1);
+}
+__device__ __forceinline__ void reduce_out(const CUtensorMap* map, uint32_t src, int c0, int c1, uint64_t pol) {
+  if constexpr (kStreamOut) tma_reduce_add_2d_hint(map, src, c0, c1, pol);
+  else tma_reduce_add_2d(map, src, c0, c1);
+}
+
 template <int BN>
 __device__ void epilogue_tile(const GemmLaunch& p, const GemmJob& job, int tile_row0, int tn, int quarter,
-                              int lane, uint32_t taddr, uint8_t* stage, bool& bad) {
+                              int lane, uint32_t taddr, uint8_t* stage, bool& bad, uint64_t pol_out) {
   const int row0 = tile_row0 + quarter * 32;  // first row handled by this warp
   if (row0 >= job.M) return;                  // all 32 rows past the edge: nothing to read or store
   const int i = row0 + lane;
@@ -213,8 +227,8 @@ __device__ void epilogue_tile(const GemmLaunch& p, const GemmJob& job, int tile_
         if (lane == 0) {
           const int x = final_trans ? row0 : j0;
           const int y = final_trans ? j0 : row0;
-          if (p.w_alpha == 0.f) tma_store_2d(&job.tmW, sbuf, x, y);
-          else tma_reduce_add_2d(&job.tmW, sbuf, x, y);
+          if (p.w_alpha == 0.f) store_out(&job.tmW, sbuf, x, y, pol_out);
+          else reduce_out(&job.tmW, sbuf, x, y, pol_out);
           bulk_commit();
         }
       } else if (row_ok) {
@@ -268,11 +282,11 @@ __device__ void epilogue_tile(const GemmLaunch& p, const GemmJob& job, int tile_
     fence_async_smem();
     __syncwarp();
     if (lane == 0) {
-      tma_store_2d(&job.tmD, sbuf, j0, row0);
-      if (upper) tma_store_2d(&job.tmD, sbuf + 2048, row0, j0);
+      store_out(&job.tmD, sbuf, j0, row0, pol_out);
+      if (upper) store_out(&job.tmD, sbuf + 2048, row0, j0, pol_out);
       if (has_d2 && !on_diag) {
-        tma_store_2d(&job.tmD2, sbuf, j0, row0);
-        if (upper) tma_store_2d(&job.tmD2, sbuf + 2048, row0, j0);
+        store_out(&job.tmD2, sbuf, j0, row0, pol_out);
+        if (upper) store_out(&job.tmD2, sbuf + 2048, row0, j0, pol_out);
       }
       bulk_commit();
     }
@@ -289,7 +303,7 @@ __device__ void epilogue_tile(const GemmLaunch& p, const GemmJob& job, int tile_
       fence_async_smem();
       __syncwarp();
       if (lane == 0) {
-        tma_store_2d(&job.tmD2, sbuf, j0, row0);
+        store_out(&job.tmD2, sbuf, j0, row0, pol_out);
         bulk_commit();
       }
     }
@@ -352,6 +366,7 @@ __device__ __forceinline__ void gemm_tc_body(const GemmLaunch& p) {
       bool ok = true;
       // The leader's full barriers as seen from either CTA of a pair (consecutive 8-byte words).
       const uint32_t full_leader = kPair ? map_shared(smem_u32(&full[0]), 0) : 0u;
+      const uint64_t pol_keep = l2_policy_evict_last();
       for (int t = unit; ok && t < p.ntiles; t += nunits) {
         const TileRef tr = tile_at(p, t, BN, C::kTileM);
         if (tr.skip) continue;
@@ -371,22 +386,31 @@ __device__ __forceinline__ void gemm_tc_body(const GemmLaunch& p) {
             // Both CTAs' copies complete on the leader's full barrier; the leader expects both.
             const uint32_t bar = full_leader + 8u * static_cast<uint32_t>(stage);
             if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * C::kStageBytes);
-            tma_load_2d_pair(sa, &job->tmA, kb * kBK, m0, bar);
+            if constexpr (kKeepA) tma_load_2d_pair_hint(sa, &job->tmA, kb * kBK, m0, bar, pol_keep);
+            else tma_load_2d_pair(sa, &job->tmA, kb * kBK, m0, bar);
             if (!bmn) {
-              tma_load_2d_pair(sb, &job->tmB, kb * kBK, n0, bar);
+              if constexpr (kKeepB) tma_load_2d_pair_hint(sb, &job->tmB, kb * kBK, n0, bar, pol_keep);
+              else tma_load_2d_pair(sb, &job->tmB, kb * kBK, n0, bar);
             } else {
 #pragma unroll
-              for (int q = 0; q < C::kBRows / 64; ++q)
-                tma_load_2d_pair(sb + q * 8192, &job->tmB, n0 + q * 64, kb * kBK, bar);
+              for (int q = 0; q < C::kBRows / 64; ++q) {
+                if constexpr (kKeepB) tma_load_2d_pair_hint(sb + q * 8192, &job->tmB, n0 + q * 64, kb * kBK, bar, pol_keep);
+                else tma_load_2d_pair(sb + q * 8192, &job->tmB, n0 + q * 64, kb * kBK, bar);
+              }
             }
           } else {
             mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
-            tma_load_2d(sa, &job->tmA, kb * kBK, m0, &full[stage]);
+            if constexpr (kKeepA) tma_load_2d_hint(sa, &job->tmA, kb * kBK, m0, &full[stage], pol_keep);
+            else tma_load_2d(sa, &job->tmA, kb * kBK, m0, &full[stage]);
             if (!bmn) {
-              tma_load_2d(sb, &job->tmB, kb * kBK, n0, &full[stage]);
+              if constexpr (kKeepB) tma_load_2d_hint(sb, &job->tmB, kb * kBK, n0, &full[stage], pol_keep);
+              else tma_load_2d(sb, &job->tmB, kb * kBK, n0, &full[stage]);
             } else {
 #pragma unroll
-              for (int q = 0; q < C::kBRows / 64; ++q) tma_load_2d(sb + q * 8192, &job->tmB, n0 + q * 64, kb * kBK, &full[stage]);
+              for (int q = 0; q < C::kBRows / 64; ++q) {
+                if constexpr (kKeepB) tma_load_2d_hint(sb + q * 8192, &job->tmB, n0 + q * 64, kb * kBK, &full[stage], pol_keep);
+                else tma_load_2d(sb + q * 8192, &job->tmB, n0 + q * 64, kb * kBK, &full[stage]);
+              }
             }
           }
           issued |= 1u << stage;
@@ -479,6 +503,7 @@ __device__ __forceinline__ void gemm_tc_body(const GemmLaunch& p) {
   } else {
     // ------------------------------------------------------------------ epilogue (warps 2..5)
     const int quarter = warp & 3;  // TMEM lanes this warp may access
+    const uint64_t pol_out = l2_policy_evict_first();
     int acc = 0;
     uint32_t acc_phase = 0;
     bool bad = false;
@@ -492,7 +517,7 @@ __device__ __forceinline__ void gemm_tc_body(const GemmLaunch& p) {
       const uint32_t taddr =
           tmem_base + static_cast<uint32_t>(acc * BN) + (static_cast<uint32_t>(quarter * 32) << 16);
       epilogue_tile<BN>(p, *tr.job, tr.tm * C::kTileM + static_cast<int>(rank) * kBM, tr.tn, quarter, lane, taddr,
-                        epi_stage + (warp - 2) * 4096, bad);
+                        epi_stage + (warp - 2) * 4096, bad, pol_out);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
