@@ -37,7 +37,7 @@ LR, BETA, EPS = 0.02, 0.95, 1e-7
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--backend", default="gram", choices=["gram", "direct", "auto"])
@@ -84,12 +84,12 @@ def restart_list(args):
     return tuple(int(x) for x in args.restarts.split(",") if x.strip() != "")
 
 
-def total_flops(shapes, backend, restarts=(2,)):
+def total_flops(shapes, backend, restarts=(2,), dense=False):
     import newton_schulz_momentum_gb300 as dm
 
     def one(r, c):
         direct = backend == "direct" or (backend == "auto" and dm.auto_uses_direct(r, c))
-        return dm.direct_flops(r, c) if direct else dm.gram_flops(r, c, 5, restarts)
+        return dm.direct_flops(r, c, dense=dense) if direct else dm.gram_flops(r, c, 5, restarts, dense=dense)
     return sum(one(r, c) for _, r, c in shapes)
 
 
@@ -375,21 +375,34 @@ def run_native(args):
             dist.barrier()
         torch.cuda.synchronize(dev)
 
-    # ---- device-resident timed region
+    # ---- device-resident timed region (an event before every step for the per-step spread)
     dm.timing_enable(True)
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    marks = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
     barrier()
     with ClockSampler(local) as clocks:
         start.record(stream)
-        for _ in range(args.steps):
+        for i in range(args.steps):
+            marks[i].record(stream)
             step()
+        marks[args.steps].record(stream)
         stop.record(stream)
         barrier()
-    kernel_times = dm.timing_read()
+    launch_list = dm.timing_read_launches(64 * args.steps + 64)
     dm.timing_enable(False)
     dm.check_status(stream)
+    exec_flops, exec_tiles, _ = dm.plan_info()
     ms_step = max_over_ranks(start.elapsed_time(stop), dev) / args.steps
     value = whole_job_tflops(flops_step, world, ms_step)
+    per_step = sorted(marks[i].elapsed_time(marks[i + 1]) for i in range(args.steps))
+    kernel_times = {c: (sum(ms for k, ms in launch_list if k == c), sum(1 for k, _ in launch_list if k == c))
+                    for c in dm.TIMING_CLASSES}
+    # per launch position within a step (the phases, in order): median over the timed steps
+    phases = None
+    if launch_list and len(launch_list) % args.steps == 0:
+        lps = len(launch_list) // args.steps
+        phases = [[launch_list[j][0], statistics.median(launch_list[i * lps + j][1] for i in range(args.steps))]
+                  for j in range(lps)]
 
     # ---- end to end through the public call: pinned host gradients in, norms out
     e2e = None
@@ -440,6 +453,16 @@ def run_native(args):
                             "achieved_gbs": (sum(r * c for _, r, c in shapes) * rw_bytes * args.steps / (rw_ms * 1e-3) / 1e9)
                             if rw_ms > 0 else None, "peak_gbs": hbm},
             "ns_tflops_frac_of_peak": value / world / tc_sust,
+            "step_ms": {"p50": statistics.median(per_step), "p90": per_step[min(len(per_step) - 1,
+                                                                             int(0.9 * len(per_step)))],
+                        "min": per_step[0], "max": per_step[-1]},
+            "phases_ms_p50": phases,
+            "dense_tflops": whole_job_tflops(total_flops(shapes, args.backend, restart_list(args), dense=True),
+                                             world, ms_step),
+            "executed": ({"tflop_per_step": exec_flops / 1e12, "tiles_per_step": exec_tiles,
+                          "gemm_tflops": exec_flops * args.steps / (gemm_ms * 1e-3) / 1e12,
+                          "frac_of_peak": exec_flops * args.steps / (gemm_ms * 1e-3) / 1e12 / tc_sust}
+                         if exec_flops > 0 and gemm_ms > 0 else None),
             "owner_assignment": ownership,
         }
         print(json.dumps(line), flush=True)

@@ -286,6 +286,21 @@ DMUON_API int dmuon_check_status(void* cuda_stream);
 DMUON_API int dmuon_timing_enable(int on);
 DMUON_API int dmuon_timing_read(double* ms_out, int64_t* launches_out);
 
+/* The same record launch by launch, in launch order: ms_out[i] and class_out[i] for the first
+ * min(count, max_launches) launches (host arrays of max_launches entries; may be NULL when
+ * max_launches == 0), *count_out = the number recorded. Clears the record like dmuon_timing_read. */
+DMUON_API int dmuon_timing_read_launches(int max_launches, double* ms_out, int* class_out, int* count_out);
+
+/*
+ * What one run of the device's cached plan (the last dmuon_ns / dmuon_ns_tp / dmuon_muon_step /
+ * dmuon_muon_step_host call on this device) issues on the tensor cores: *exec_flops_out = 2 x the
+ * multiply-adds of every tile of every GEMM launch (diagonal tiles of symmetric products in full, K
+ * rounded up to the 64-wide ring slice), *tiles_out = the tiles, *gemm_launches_out = the GEMM launches.
+ * For the fused small-matrix plan exec_flops is -1 (not counted), tiles 0 and launches 1.
+ * DMUON_ERR_INVALID_ARG when nothing has been planned on the current device.
+ */
+DMUON_API int dmuon_plan_info(double* exec_flops_out, int64_t* tiles_out, int* gemm_launches_out);
+
 /* Text of the last error on the calling thread; valid until the next call on that thread. */
 DMUON_API const char* dmuon_last_error(void);
 

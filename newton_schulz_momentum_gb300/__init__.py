@@ -45,6 +45,7 @@ EXPORTS = (
     "dmuon_last_error", "dmuon_version", "dmuon_set_workspace_limit", "dmuon_workspace_size",
     "dmuon_release_workspace", "dmuon_timing_enable", "dmuon_timing_read", "dmuon_momentum_normalize_noalloc",
     "dmuon_assign_owners", "dmuon_adamw_step", "dmuon_ns_tp", "dmuon_muon_step_host",
+    "dmuon_timing_read_launches", "dmuon_plan_info",
 )
 COST_MODELS = {"elements": 0, "gram_flops": 1, "direct_flops": 2}
 NOALLOC_MAX_ELEMS = 268435456
@@ -97,6 +98,8 @@ def lib():
     L.dmuon_adamw_step.argtypes = [i32, _c_vpp, _c_vpp, i32, _c_vpp, _c_vpp, _c_i64p, f64, f64, f64, f64, f64, i32, vp]
     L.dmuon_assign_owners.argtypes = [i32, _c_i64p, _c_i64p, _c_ip, i32, i32, _c_ip, ctypes.POINTER(ctypes.c_double)]
     L.dmuon_timing_read.argtypes = [ctypes.POINTER(ctypes.c_double), _c_i64p]
+    L.dmuon_timing_read_launches.argtypes = [i32, ctypes.POINTER(ctypes.c_double), _c_ip, _c_ip]
+    L.dmuon_plan_info.argtypes = [ctypes.POINTER(ctypes.c_double), _c_i64p, _c_ip]
     for name in EXPORTS:
         if name not in ("dmuon_last_error", "dmuon_version"):
             getattr(L, name).restype = ctypes.c_int
@@ -367,6 +370,24 @@ def timing_read():
     return {c: (ms[i], n[i]) for i, c in enumerate(TIMING_CLASSES)}
 
 
+def timing_read_launches(max_launches=4096):
+    """[(class, milliseconds)] launch by launch, in launch order, since the last read (at most
+    max_launches are returned); waits for the recorded events and clears the record."""
+    ms = (ctypes.c_double * max_launches)()
+    cls = (ctypes.c_int * max_launches)()
+    n = ctypes.c_int()
+    _check(lib().dmuon_timing_read_launches(max_launches, ms, cls, ctypes.byref(n)))
+    return [(TIMING_CLASSES[cls[i]] if 0 <= cls[i] < len(TIMING_CLASSES) else str(cls[i]), ms[i])
+            for i in range(min(n.value, max_launches))]
+
+
+def plan_info():
+    """(executed MMA flops, tiles, GEMM launches) of one run of the current device's cached plan."""
+    f, t, n = ctypes.c_double(), ctypes.c_int64(), ctypes.c_int()
+    _check(lib().dmuon_plan_info(ctypes.byref(f), ctypes.byref(t), ctypes.byref(n)))
+    return f.value, t.value, n.value
+
+
 def assign_owners(shapes, nranks, layer_ids=None, cost="gram_flops"):
     """Dedicated ownership by LPT (host-only): returns (owner rank per matrix, summed cost per rank)."""
     n = len(shapes)
@@ -383,23 +404,25 @@ def release_workspace():
     _check(lib().dmuon_release_workspace())
 
 
-def gram_flops(m, n, steps=5, restarts=DEFAULT_RESTARTS):
+def gram_flops(m, n, steps=5, restarts=DEFAULT_RESTARTS, dense=False):
     """Algorithmic flops of Gram NS as implemented, on one matrix (m <= n after orientation), every
     symmetric product counted at half: X X^T m^2 n; per step R^2 m^3, the Q update Z Q 2 m^3 unless right
     after a (re)start, the R update (S = (aI+Z) R and R = S (aI+Z), both symmetric) 2 m^3 when the next
     step exists and is not a restart; restart Q X 2 m^2 n + X X^T m^2 n; output Q X 2 m^2 n. With the
-    default 5 steps and restart [2]: 6 m^2 n + 17 m^3."""
+    default 5 steps and restart [2]: 6 m^2 n + 17 m^3. dense=True counts the symmetric products in full
+    (8 m^2 n + 28 m^3 with the defaults), the count a general GEMM would execute."""
     m, n = min(m, n), max(m, n)
+    h = 2 if dense else 1  # symmetric products: half, or in full
     rs = {k for k in restarts if 0 < k < steps}
-    f, fresh = m * m * n, True
+    f, fresh = h * m * m * n, True
     for k in range(steps):
         if k in rs:
-            f += 3 * m * m * n
+            f += 2 * m * m * n + h * m * m * n
             fresh = True
-        f += m ** 3 + (0 if fresh else 2 * m ** 3)
+        f += h * m ** 3 + (0 if fresh else 2 * m ** 3)
         fresh = False
         if k + 1 < steps and (k + 1) not in rs:
-            f += 2 * m ** 3
+            f += 2 * h * m ** 3
     return f + 2 * m * m * n
 
 
@@ -409,8 +432,9 @@ def auto_uses_direct(m, n):
     return 3 * n < 4 * m
 
 
-def direct_flops(m, n, steps=5):
+def direct_flops(m, n, steps=5, dense=False):
     """Algorithmic flops of direct NS on one matrix, symmetric products at half: per step
-    X X^T m^2 n, A^2 m^3, B X 2 m^2 n."""
+    X X^T m^2 n, A^2 m^3, B X 2 m^2 n (dense=True: the symmetric ones in full, 4 m^2 n + 2 m^3)."""
     m, n = min(m, n), max(m, n)
-    return steps * (3 * m * m * n + m ** 3)
+    h = 2 if dense else 1
+    return steps * ((h + 2) * m * m * n + h * m ** 3)

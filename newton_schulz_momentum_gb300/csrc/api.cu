@@ -137,6 +137,10 @@ struct Plan {
   // Tensor-parallel emulation (kPlanNsTp): shard boundaries along the long side.
   std::vector<int64_t> shard_bounds;
   int tp_slabs = 0;
+  // MMA work one run of the plan issues: every tile of every GEMM launch, K rounded up to the 64-wide
+  // ring slice (dmuon_plan_info). -1 for the fused small-matrix plan, which is not tile-based.
+  double exec_flops = 0.0;
+  int64_t exec_tiles = 0;
 };
 
 struct Layout {
@@ -587,6 +591,7 @@ int build_plan_host(Plan& pl, const PlanKey& key, const std::vector<const void*>
   }
   if (pl.small_fused) {
     pl.off_small = lay.take(sizeof(SmallJob) * nm, 256);
+    pl.exec_flops = -1.0;
   } else if (key.kind != kPlanMomNorm) {
     for (size_t g = 0; g + 1 < pl.group_begin.size(); ++g) {
       std::vector<int> idx_gram, idx_direct;
@@ -650,12 +655,16 @@ int build_plan_host(Plan& pl, const PlanKey& key, const std::vector<const void*>
       // operands.
       const int64_t a_bytes = static_cast<int64_t>(js.M) * js.K * 2;
       const int band = a_bytes <= (int64_t(40) << 20) ? tm_n : std::min(tm_n, 8);
+      const size_t before = pl.tiles.size();
       for (int g0 = 0; g0 < tm_n; g0 += band)
         for (int tn = 0; tn < tn_n; ++tn)
           for (int tm = g0; tm < std::min(g0 + band, tm_n); ++tm) {
             if ((js.flags & kJobSymmetric) && tn * tw + tw - 1 < tm * th) continue;
             pl.tiles.push_back(GemmTile{j, tm, tn, 0});
           }
+      const int64_t jt = static_cast<int64_t>(pl.tiles.size() - before);
+      pl.exec_tiles += jt;
+      pl.exec_flops += 2.0 * static_cast<double>(jt) * th * tw * static_cast<double>(round_up(js.K, kBK));
     }
     L.ntiles = static_cast<int>(pl.tiles.size()) - L.first_tile;
     pl.launches.push_back(L);
@@ -1319,6 +1328,46 @@ int dmuon_timing_read(double* ms_out, int64_t* launches_out) {
   }
   g_timed.clear();
   return st;
+}
+
+int dmuon_timing_read_launches(int max_launches, double* ms_out, int* class_out, int* count_out) {
+  if (!count_out || max_launches < 0 || (max_launches > 0 && (!ms_out || !class_out)))
+    return fail(DMUON_ERR_INVALID_ARG, "output arrays are NULL or max_launches is negative");
+  std::lock_guard<std::mutex> lock(g_mu);
+  int st = DMUON_OK;
+  int i = 0;
+  for (auto& t : g_timed) {
+    float ms = 0.f;
+    cudaError_t e = cudaEventSynchronize(t.stop);
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, t.start, t.stop);
+    if (e != cudaSuccess && st == DMUON_OK) st = cuda_fail(e, "timing events");
+    if (i < max_launches) {
+      ms_out[i] = ms;
+      class_out[i] = t.cls;
+    }
+    ++i;
+    g_event_pool.push_back(t.start);
+    g_event_pool.push_back(t.stop);
+  }
+  *count_out = i;
+  g_timed.clear();
+  return st;
+}
+
+int dmuon_plan_info(double* exec_flops_out, int64_t* tiles_out, int* gemm_launches_out) {
+  if (!exec_flops_out || !tiles_out || !gemm_launches_out) return fail(DMUON_ERR_INVALID_ARG, "outputs are NULL");
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState* ds = nullptr;
+  int st = current_device(&ds);
+  if (st != DMUON_OK) return st;
+  if (!ds->plan.bound) return fail(DMUON_ERR_INVALID_ARG, "no call has been planned on this device");
+  const Plan& pl = ds->plan;
+  *exec_flops_out = pl.exec_flops;
+  *tiles_out = pl.exec_tiles;
+  int n = 0;
+  for (const LaunchRec& L : pl.launches) n += L.tp_reduce ? 0 : 1;
+  *gemm_launches_out = pl.small_fused ? 1 : n;
+  return DMUON_OK;
 }
 
 const char* dmuon_last_error(void) { return t_last_error.c_str(); }

@@ -364,3 +364,26 @@ def test_llama_whole_model(dm, backend):
         names |= {"layers.31.up_proj", "layers.0.down_proj"}
     _llama_run(dm, 32, 6, names, backend)
     dm.release_workspace()
+
+
+def test_plan_info_and_launch_timing(dm):
+    """dmuon_plan_info and the per-launch timing record agree with the plan that ran: the GEMM launches
+    counted both ways match, and the executed MMA flops lie between the algorithmic count (symmetric
+    products at half) and the dense count padded to whole 256 x 256 tiles and 64-wide K slices."""
+    shapes = [(520, 264), (264, 1040), (1024, 256), (300, 300)]
+    W = [cuda(workloads.gaussian(s, 0.02, 60 + i)) for i, s in enumerate(shapes)]
+    G = [cuda(workloads.gaussian(s, 1.0, 65 + i)) for i, s in enumerate(shapes)]
+    M = [torch.zeros(s, dtype=torch.float32, device="cuda") for s in shapes]
+    dm.timing_enable(True)
+    dm.muon_step(W, G, M, lr=0.02, beta=0.95, coeffs=dm.YOU, restarts=(2,), backend="gram")
+    rec = dm.timing_read_launches()
+    dm.timing_enable(False)
+    dm.check_status()
+    flops, tiles, gemm_launches = dm.plan_info()
+    assert sum(1 for c, _ in rec if c == "gemm_tc") == gemm_launches > 0
+    assert [c for c, _ in rec[:3]] == ["momentum_sumsq", "finalize_norms", "normalize_cast"]
+    assert all(ms >= 0 for _, ms in rec)
+    algo = sum(dm.gram_flops(r, c) for r, c in shapes)
+    padded = sum(dm.gram_flops(-(-min(r, c) // 256) * 256, -(-max(r, c) // 256) * 256, dense=True)
+                 for r, c in shapes)
+    assert tiles > 0 and algo <= flops <= padded
