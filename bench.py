@@ -264,6 +264,27 @@ def max_over_ranks(ms, device):
     return float(t.item())
 
 
+def live_copy_rate(dev):
+    """This box's copy bandwidth measured the way the peaks file was (b.copy_(a) over 1 Gi bf16 elements,
+    read + write bytes, best of 10): the row-wise passes are compared against it as well."""
+    import torch
+    a = torch.empty(1 << 30, dtype=torch.bfloat16, device=dev)
+    b = torch.empty_like(a)
+    a.fill_(1.0)
+    best = None
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for _ in range(11):
+        e0.record()
+        b.copy_(a)
+        e1.record()
+        e1.synchronize()
+        ms = e0.elapsed_time(e1)
+        best = ms if best is None else min(best, ms)
+    del a, b
+    torch.cuda.empty_cache()
+    return 2 * 2 * (1 << 30) / (best * 1e-3) / 1e9
+
+
 def whole_job_tflops(flops_per_rank_step, world, ms_per_step):
     """Weak scaling: every rank updates its own full matrix set, so the job does world x the work."""
     return world * flops_per_rank_step / (ms_per_step * 1e-3) / 1e12
@@ -369,6 +390,7 @@ def run_native(args):
     for _ in range(args.warmup):
         step()
     dm.check_status(stream)
+    live_copy_gbs = live_copy_rate(dev)
 
     def barrier():
         if world > 1:
@@ -451,7 +473,8 @@ def run_native(args):
             "launches_per_step": {k: v[1] / args.steps for k, v in kernel_times.items()},
             "rowwise_hbm": {"bytes_per_step": sum(r * c for _, r, c in shapes) * rw_bytes,
                             "achieved_gbs": (sum(r * c for _, r, c in shapes) * rw_bytes * args.steps / (rw_ms * 1e-3) / 1e9)
-                            if rw_ms > 0 else None, "peak_gbs": hbm},
+                            if rw_ms > 0 else None, "peak_gbs": hbm,
+                            "copy_gbs_this_box": live_copy_gbs},
             "ns_tflops_frac_of_peak": value / world / tc_sust,
             "step_ms": {"p50": statistics.median(per_step), "p90": per_step[min(len(per_step) - 1,
                                                                              int(0.9 * len(per_step)))],

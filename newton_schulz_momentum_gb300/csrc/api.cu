@@ -771,6 +771,7 @@ int run_plan(DeviceState& ds, const Plan& pl, const float* coeffs, float lr, flo
   rl.norms_out = norms_out;
   rl.beta = beta;
   rl.eps = eps;
+  rl.status = ds.status;
   const GemmJob* jobs = reinterpret_cast<const GemmJob*>(base + pl.off_jobs);
   const GemmTile* tiles = reinterpret_cast<const GemmTile*>(base + pl.off_tiles);
   const bool overwrite = pl.key.kind == kPlanNs || pl.key.kind == kPlanNsTp;  // W = O, not W -= lr O

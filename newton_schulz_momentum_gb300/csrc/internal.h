@@ -175,6 +175,9 @@ struct RowLaunch {
   // `inv` and `norms_out` then point at the group's first entry, and block b works on momentum chunk
   // chunk_base + b (cast tile tile_base + b) of the plan-wide numbering. Zero for a whole-plan launch.
   int64_t chunk_base = 0, tile_base = 0;
+  // Device status word for bounded waits. With it the momentum pass streams M and G through a
+  // shared-memory ring of bulk copies; without it (the allocation-free entry) it uses vector loads.
+  unsigned* status = nullptr;
 };
 
 // ------------------------------------------------------------------------------------------------

@@ -7,6 +7,7 @@
 //                       transposed through shared memory) -- the fp16 input of the iteration.
 // Reductions are deterministic: fixed chunking, fixed tree order, no atomics.
 #include "internal.h"
+#include "tc_ptx.h"
 
 namespace dmuon {
 namespace {
@@ -119,6 +120,124 @@ __global__ void __launch_bounds__(kThreads) momentum_sumsq_kernel(const RowLaunc
     scalar_from = vend;
   }
   for (int64_t e = scalar_from + threadIdx.x; e < end; e += kThreads) {
+    float m = mt.M[e];
+    if (has_g) {
+      m = fmaf(beta, m, load1_grad(mt.G, mt.gdtype, e));
+      mt.M[e] = m;
+    }
+    acc = fmaf(m, m, acc);
+  }
+  const float total = block_sum(acc, red);
+  if (threadIdx.x == 0) p.partials[mt.part_begin + local] = total;
+}
+
+// The momentum pass streamed through shared memory: one thread moves 4096-element slices of M and G
+// into a ring of kRingSlots slots with bulk copies (cp.async.bulk, completion on an mbarrier), and the
+// CTA updates M from the slot and writes it back with coalesced 16-byte stores. The bytes in flight are
+// set by the ring, not by registers: up to 3 x 24 KB per CTA with bf16 gradients, two CTAs per SM. Every
+// wait is bounded; on expiry the CTA sets kDevTimeout, lets its copies land and returns.
+constexpr int kSub = 4096;       // elements per ring slot
+constexpr int kRingSlots = 3;
+constexpr int kSlotBytes = kSub * 4 * 2;  // M (fp32) and G (up to fp32)
+constexpr int kBulkSmem = kRingSlots * kSlotBytes + 64;
+static_assert(kChunkElems % kSub == 0, "a chunk is a whole number of slots");
+
+__global__ void __launch_bounds__(kThreads, 2) momentum_sumsq_bulk_kernel(const RowLaunch p) {
+  extern __shared__ __align__(128) uint8_t ring[];
+  __shared__ float red[kThreads / 32];
+  uint64_t* full = reinterpret_cast<uint64_t*>(ring + kRingSlots * kSlotBytes);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(full + kRingSlots);
+  const int64_t chunk = p.chunk_base + blockIdx.x;
+  const int mi = find_matrix(p.chunk_prefix, p.nmats, chunk);
+  const RowMat mt = p.mats[mi];
+  const int64_t local = chunk - p.chunk_prefix[mi];
+  const int64_t numel = mt.rows * mt.cols;
+  const int64_t begin = local * kChunkElems;
+  const int64_t end = min(begin + static_cast<int64_t>(kChunkElems), numel);
+  const bool has_g = mt.G != nullptr;
+  const int gsize = mt.gdtype == 1 ? 2 : 4;
+  const float beta = p.beta;
+  // Slices cover a multiple of 8 elements (whole 16-byte units of either gradient type); the last
+  // few elements of a matrix go through plain loads below.
+  // Rows that are not 16-byte vectorisable never reach the bulk copies (plain loads for the whole chunk).
+  const int64_t nbulk = mt.vec_ok ? ((end - begin) & ~int64_t(7)) : 0;
+  const int nsub = static_cast<int>((nbulk + kSub - 1) / kSub);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kRingSlots; ++s) ptx::mbar_init(&full[s], 1);
+    *abort_flag = 0;
+    ptx::fence_barrier_init();
+  }
+  __syncthreads();
+  uint64_t policy = 0;
+  if (threadIdx.x == 0) policy = ptx::l2_policy_evict_first();
+  auto issue = [&](int i) {  // thread 0: slice i into slot i % kRingSlots
+    const int s = i % kRingSlots;
+    const int64_t e0 = begin + static_cast<int64_t>(i) * kSub;
+    const uint32_t cnt = static_cast<uint32_t>(min(static_cast<int64_t>(kSub), nbulk - static_cast<int64_t>(i) * kSub));
+    const uint32_t mb = cnt * 4u, gb = has_g ? cnt * static_cast<uint32_t>(gsize) : 0u;
+    uint8_t* slot = ring + s * kSlotBytes;
+    ptx::mbar_arrive_expect_tx(&full[s], mb + gb);
+    ptx::bulk_load_hint(ptx::smem_u32(slot), mt.M + e0, mb, &full[s], policy);
+    if (has_g)
+      ptx::bulk_load_hint(ptx::smem_u32(slot + kSub * 4), static_cast<const uint8_t*>(mt.G) + e0 * gsize, gb, &full[s],
+                          policy);
+  };
+  int issued = 0;
+  if (threadIdx.x == 0)
+    for (; issued < min(kRingSlots, nsub); ++issued) issue(issued);
+
+  float acc = 0.f;
+  bool ok = true;
+  int done = 0;
+  for (; done < nsub; ++done) {
+    const int s = done % kRingSlots;
+    const uint32_t parity = static_cast<uint32_t>(done / kRingSlots) & 1u;
+    const bool got = ptx::wait_bounded(&full[s], parity, abort_flag, p.status, ptx::kWaitLimitNs, true);
+    if (!__syncthreads_and(got)) {
+      ok = false;
+      break;
+    }
+    const int64_t e0 = begin + static_cast<int64_t>(done) * kSub;
+    const int cnt4 = static_cast<int>(min(static_cast<int64_t>(kSub), nbulk - static_cast<int64_t>(done) * kSub)) / 4;
+    const float4* sm = reinterpret_cast<const float4*>(ring + s * kSlotBytes);
+    const uint8_t* sg = ring + s * kSlotBytes + kSub * 4;
+    for (int q = threadIdx.x; q < cnt4; q += kThreads) {
+      float4 m = sm[q];
+      if (has_g) {
+        float g[4];
+        if (mt.gdtype == 1) {
+          const uint2 u = reinterpret_cast<const uint2*>(sg)[q];
+          g[0] = __uint_as_float(u.x << 16), g[1] = __uint_as_float(u.x & 0xFFFF0000u);
+          g[2] = __uint_as_float(u.y << 16), g[3] = __uint_as_float(u.y & 0xFFFF0000u);
+        } else {
+          const float4 v = reinterpret_cast<const float4*>(sg)[q];
+          g[0] = v.x, g[1] = v.y, g[2] = v.z, g[3] = v.w;
+        }
+        m.x = fmaf(beta, m.x, g[0]);
+        m.y = fmaf(beta, m.y, g[1]);
+        m.z = fmaf(beta, m.z, g[2]);
+        m.w = fmaf(beta, m.w, g[3]);
+        __stcs(reinterpret_cast<float4*>(mt.M + e0) + q, m);
+      }
+      acc = fmaf(m.x, m.x, acc);
+      acc = fmaf(m.y, m.y, acc);
+      acc = fmaf(m.z, m.z, acc);
+      acc = fmaf(m.w, m.w, acc);
+    }
+    __syncthreads();  // every thread is done with slot s
+    if (threadIdx.x == 0 && issued < nsub) issue(issued++);
+  }
+  if (!ok) {
+    // Let every copy already issued land before the CTA's shared memory is released.
+    if (threadIdx.x == 0)
+      for (int i = done; i < issued; ++i)
+        ptx::wait_bounded(&full[i % kRingSlots], static_cast<uint32_t>(i / kRingSlots) & 1u, abort_flag, p.status,
+                          ptx::kDrainLimitNs, false);
+    __syncthreads();
+    return;
+  }
+  for (int64_t e = begin + nbulk + threadIdx.x; e < end; e += kThreads) {
     float m = mt.M[e];
     if (has_g) {
       m = fmaf(beta, m, load1_grad(mt.G, mt.gdtype, e));
@@ -296,7 +415,14 @@ cudaError_t launch_tp_reduce(const TpReduceLaunch& p, cudaStream_t stream) {
 
 cudaError_t launch_momentum_sumsq(const RowLaunch& p, int64_t nchunks, cudaStream_t stream) {
   if (nchunks <= 0) return cudaSuccess;
-  momentum_sumsq_kernel<<<static_cast<unsigned>(nchunks), kThreads, 0, stream>>>(p);
+  if (p.status) {
+    cudaError_t e = cudaFuncSetAttribute(momentum_sumsq_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kBulkSmem);
+    if (e != cudaSuccess) return e;
+    momentum_sumsq_bulk_kernel<<<static_cast<unsigned>(nchunks), kThreads, kBulkSmem, stream>>>(p);
+  } else {
+    momentum_sumsq_kernel<<<static_cast<unsigned>(nchunks), kThreads, 0, stream>>>(p);
+  }
   return cudaGetLastError();
 }
 

@@ -294,6 +294,17 @@ __device__ __forceinline__ void tma_reduce_add_2d_hint(const CUtensorMap* map, u
       : "memory");
 }
 
+// Untiled bulk copy from global memory into this CTA's shared memory, completing `bytes` on `bar`
+// (both addresses 16-byte aligned, bytes a multiple of 16), streamed through L2 with `policy`.
+__device__ __forceinline__ void bulk_load_hint(uint32_t smem_dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                               uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+          smem_dst),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
