@@ -301,6 +301,17 @@ DMUON_API int dmuon_timing_read_launches(int max_launches, double* ms_out, int* 
  */
 DMUON_API int dmuon_plan_info(double* exec_flops_out, int64_t* tiles_out, int* gemm_launches_out);
 
+/*
+ * Diagnostic for the library's failure detection (no counterpart on the pages). Every mbarrier wait in
+ * the library's kernels is bounded: when one exceeds its limit the kernel records DMUON_ERR_TIMEOUT in the
+ * device status word, drains its own copies, frees its tensor memory and returns, leaving the CUDA
+ * context usable. This launches one CTA whose wait, through that same bounded wait, is on a phase that
+ * nothing completes, with a limit of limit_ns in [1e6, 2e9] nanoseconds; afterwards
+ * dmuon_check_status(cuda_stream) returns DMUON_ERR_TIMEOUT (and clears it). Faults and traps are never
+ * used.
+ */
+DMUON_API int dmuon_selftest_bounded_wait(int64_t limit_ns, void* cuda_stream);
+
 /* Text of the last error on the calling thread; valid until the next call on that thread. */
 DMUON_API const char* dmuon_last_error(void);
 

@@ -45,7 +45,7 @@ EXPORTS = (
     "dmuon_last_error", "dmuon_version", "dmuon_set_workspace_limit", "dmuon_workspace_size",
     "dmuon_release_workspace", "dmuon_timing_enable", "dmuon_timing_read", "dmuon_momentum_normalize_noalloc",
     "dmuon_assign_owners", "dmuon_adamw_step", "dmuon_ns_tp", "dmuon_muon_step_host",
-    "dmuon_timing_read_launches", "dmuon_plan_info",
+    "dmuon_timing_read_launches", "dmuon_plan_info", "dmuon_selftest_bounded_wait",
 )
 COST_MODELS = {"elements": 0, "gram_flops": 1, "direct_flops": 2}
 NOALLOC_MAX_ELEMS = 268435456
@@ -100,6 +100,7 @@ def lib():
     L.dmuon_timing_read.argtypes = [ctypes.POINTER(ctypes.c_double), _c_i64p]
     L.dmuon_timing_read_launches.argtypes = [i32, ctypes.POINTER(ctypes.c_double), _c_ip, _c_ip]
     L.dmuon_plan_info.argtypes = [ctypes.POINTER(ctypes.c_double), _c_i64p, _c_ip]
+    L.dmuon_selftest_bounded_wait.argtypes = [i64, vp]
     for name in EXPORTS:
         if name not in ("dmuon_last_error", "dmuon_version"):
             getattr(L, name).restype = ctypes.c_int
@@ -379,6 +380,12 @@ def timing_read_launches(max_launches=4096):
     _check(lib().dmuon_timing_read_launches(max_launches, ms, cls, ctypes.byref(n)))
     return [(TIMING_CLASSES[cls[i]] if 0 <= cls[i] < len(TIMING_CLASSES) else str(cls[i]), ms[i])
             for i in range(min(n.value, max_launches))]
+
+
+def selftest_bounded_wait(seconds=0.05, stream=None):
+    """Launch one bounded wait that cannot complete (limit `seconds`): the next check_status() raises
+    DmuonError with status ERR_TIMEOUT, exactly as when one of the library's waits runs out."""
+    _check(lib().dmuon_selftest_bounded_wait(int(seconds * 1e9), _stream(stream)))
 
 
 def plan_info():

@@ -1355,6 +1355,18 @@ int dmuon_timing_read_launches(int max_launches, double* ms_out, int* class_out,
   return st;
 }
 
+int dmuon_selftest_bounded_wait(int64_t limit_ns, void* cuda_stream) {
+  if (limit_ns < 1000000 || limit_ns > 2000000000)
+    return fail(DMUON_ERR_INVALID_ARG, "limit_ns must be in [1e6, 2e9] (1 ms to 2 s)");
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState* ds = nullptr;
+  int st = current_device(&ds);
+  if (st != DMUON_OK) return st;
+  cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
+  DM_CUDA(launch_selftest_wait(ds->status, static_cast<unsigned long long>(limit_ns), stream), "self-test launch");
+  return DMUON_OK;
+}
+
 int dmuon_plan_info(double* exec_flops_out, int64_t* tiles_out, int* gemm_launches_out) {
   if (!exec_flops_out || !tiles_out || !gemm_launches_out) return fail(DMUON_ERR_INVALID_ARG, "outputs are NULL");
   std::lock_guard<std::mutex> lock(g_mu);

@@ -235,6 +235,8 @@ struct TpReduceLaunch {
 cudaError_t launch_shard_sumsq(const ShardSumsqLaunch& p, cudaStream_t stream);
 cudaError_t launch_tp_reduce(const TpReduceLaunch& p, cudaStream_t stream);
 
+// Diagnostic: one bounded wait on an mbarrier phase that nothing completes (records kDevTimeout).
+cudaError_t launch_selftest_wait(unsigned* status, unsigned long long limit_ns, cudaStream_t stream);
 cudaError_t launch_momentum_sumsq(const RowLaunch& p, int64_t nchunks, cudaStream_t stream);
 cudaError_t launch_finalize_norms(const RowLaunch& p, cudaStream_t stream);
 cudaError_t launch_normalize_cast(const RowLaunch& p, int64_t ntiles, cudaStream_t stream);

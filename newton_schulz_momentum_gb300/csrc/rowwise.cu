@@ -401,6 +401,20 @@ __global__ void __launch_bounds__(kThreads) tp_reduce_kernel(const TpReduceLaunc
   }
 }
 
+// One thread waits, through the same bounded wait the library's kernels use, on an mbarrier phase that
+// nothing completes: after limit_ns it gives up and records kDevTimeout in the status word.
+__global__ void selftest_wait_kernel(unsigned* status, unsigned long long limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(&bar, 1);
+    abort_flag = 0;
+    ptx::fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) ptx::wait_bounded(&bar, 0, &abort_flag, status, limit_ns, true);
+}
+
 }  // namespace
 
 cudaError_t launch_shard_sumsq(const ShardSumsqLaunch& p, cudaStream_t stream) {
@@ -410,6 +424,11 @@ cudaError_t launch_shard_sumsq(const ShardSumsqLaunch& p, cudaStream_t stream) {
 
 cudaError_t launch_tp_reduce(const TpReduceLaunch& p, cudaStream_t stream) {
   tp_reduce_kernel<<<static_cast<unsigned>(p.m), kThreads, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_selftest_wait(unsigned* status, unsigned long long limit_ns, cudaStream_t stream) {
+  selftest_wait_kernel<<<1, 32, 0, stream>>>(status, limit_ns);
   return cudaGetLastError();
 }
 

@@ -104,6 +104,10 @@ def test_invalid_arguments_rejected_without_device(L):
     rc, msg = _status(L, L.dmuon_muon_step_host(1, P, H, P, 3, P, rows, cols, None, 0.02, 0.95, c, 5, r, 1, 1, 1e-7,
                                                 0, None))
     assert rc == dm.ERR_INVALID_ARG and "grad_dtype" in msg
+    # failure-detection self-test: the limit is checked before anything touches a device
+    for bad in (0, 999999, 2000000001):
+        rc, msg = _status(L, L.dmuon_selftest_bounded_wait(bad, None))
+        assert rc == dm.ERR_INVALID_ARG and "limit_ns" in msg
 
 
 def test_flop_counts_closed_form():

@@ -1,0 +1,46 @@
+"""GPU: failure detection without a fault. The library's kernels bound every mbarrier wait; a wait that
+runs out records DMUON_ERR_TIMEOUT in the device status word and the kernel returns. The self-test makes
+one such wait run out (a phase that nothing completes, 50 ms limit) and checks that the status is
+reported once, that it clears, and that the context still computes correctly afterwards."""
+
+import time
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dm():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+    __graft_entry__.build()
+    import newton_schulz_momentum_gb300 as dm
+    return dm
+
+
+def test_bounded_wait_times_out_and_reports(dm):
+    dm.check_status()  # start clean
+    t0 = time.perf_counter()
+    dm.selftest_bounded_wait(0.05)
+    with pytest.raises(dm.DmuonError) as ei:
+        dm.check_status()
+    elapsed = time.perf_counter() - t0
+    assert ei.value.status == dm.ERR_TIMEOUT
+    assert 0.04 <= elapsed < 2.0  # the wait ran to its limit and no further
+    dm.check_status()  # the status word was cleared
+
+    # the context is still usable: a GEMM after the timeout is correct
+    rng = np.random.default_rng(3)
+    a = rng.standard_normal((256, 320)).astype(np.float16)
+    ad = torch.from_numpy(a).cuda()
+    d = torch.empty((256, 256), dtype=torch.float16, device="cuda")
+    dm.gemm_f16(ad, ad, d, b_trans=True)
+    dm.check_status()
+    want = a.astype(np.float64) @ a.astype(np.float64).T
+    got = d.float().cpu().numpy()
+    assert np.linalg.norm(got - want) <= 2e-3 * np.linalg.norm(want)
