@@ -106,10 +106,11 @@ def test_pageable_host_memory_fp32(dm):
     assert _equal(ref, got)
 
 
-def test_auto_backend_pipelined(dm):
+@pytest.mark.parametrize("backend", ["auto", "direct"])
+def test_other_backends_pipelined(dm, backend):
     steps = [_grads(SHAPES, 900, torch.bfloat16)]
-    ref = _reference(dm, SHAPES, steps, torch.bfloat16, backend="auto")
-    got = _pipelined(dm, SHAPES, steps, torch.bfloat16, 3, backend="auto")
+    ref = _reference(dm, SHAPES, steps, torch.bfloat16, backend=backend)
+    got = _pipelined(dm, SHAPES, steps, torch.bfloat16, 3, backend=backend)
     assert _equal(ref, got)
 
 
