@@ -135,8 +135,9 @@ DMUON_API int dmuon_muon_step(int count, float* const* params, const void* const
  * caller whose gradients are produced or staged on the host uses. (The pages transfer gradients between
  * ranks, not from the host; this is the single-GPU form of "gradients in, update out".) Equivalent to
  * copying every grads_host[i] into grads[i] and then calling dmuon_muon_step, with identical results,
- * but the copies overlap the computation: the matrices are taken in `groups` consecutive groups of about
- * equal gradient bytes; group g's copies run on the library's copy stream while earlier groups compute on
+ * but the copies overlap the computation: the matrices are taken in `groups` consecutive groups by
+ * gradient bytes (the first half the size of the others, since its copy is the one left exposed);
+ * group g's copies run on the library's copy stream while earlier groups compute on
  * cuda_stream, and group g's momentum pass waits only for its own copies. Each group runs its row-wise
  * passes and Newton-Schulz phases as grouped launches of its own.
  *

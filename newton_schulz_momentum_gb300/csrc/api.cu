@@ -574,7 +574,9 @@ int build_plan_host(Plan& pl, const PlanKey& key, const std::vector<const void*>
                                          : static_cast<int>(pl.chunk_prefix[i + 1] - pl.chunk_prefix[i]);
     part += r.part_count;
   }
-  // Matrix groups: consecutive runs of about equal gradient bytes (one group for every other plan).
+  // Matrix groups: consecutive runs of gradient bytes, the first holding half the share of each later
+  // one (its copy is the only one not hidden behind computation): boundary g sits at the cumulative share
+  // (2g - 1) / (2 ng - 1). One group for every other plan.
   {
     const int ng = (key.kind == kPlanMuon && !pl.small_fused) ? std::max(1, std::min(key.groups, nm)) : 1;
     pl.group_begin.assign(1, 0);
@@ -585,7 +587,7 @@ int build_plan_host(Plan& pl, const PlanKey& key, const std::vector<const void*>
       run += pl.mats[i].rows * pl.mats[i].cols;
       const int g = static_cast<int>(pl.group_begin.size());  // boundary being placed
       // Close group g - 1 after matrix i once it holds its share, leaving a matrix for each later group.
-      if (run * ng >= total * g && nm - (i + 1) >= ng - g) pl.group_begin.push_back(i + 1);
+      if (run * (2 * ng - 1) >= total * (2 * g - 1) && nm - (i + 1) >= ng - g) pl.group_begin.push_back(i + 1);
     }
     pl.group_begin.push_back(nm);
   }
