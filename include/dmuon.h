@@ -139,7 +139,11 @@ DMUON_API int dmuon_muon_step(int count, float* const* params, const void* const
  * gradient bytes (the first half the size of the others, since its copy is the one left exposed);
  * group g's copies run on the library's copy stream while earlier groups compute on
  * cuda_stream, and group g's momentum pass waits only for its own copies. Each group runs its row-wise
- * passes and Newton-Schulz phases as grouped launches of its own.
+ * passes and Newton-Schulz phases as grouped launches of its own. With many small matrices (64 or more
+ * averaging under 4 MiB of gradient), where one copy per matrix would cost the host more than the
+ * transfers, one gather launch on cuda_stream reads every gradient out of host memory instead (the
+ * memory must then be device-readable: page-locked, or pageable on devices that read host page tables;
+ * otherwise the copies above are used) and the step runs as one group.
  *
  *   grads_host  host array of `count` host pointers to the gradients (rows[i] x cols[i], `grad_dtype`,
  *               row-major, contiguous). For the copies to overlap they must be page-locked

@@ -55,6 +55,10 @@ int cuda_fail(cudaError_t e, const char* what) {
 constexpr size_t kNone = ~size_t(0);
 constexpr int64_t kMaxDim = int64_t(1) << 24;
 constexpr int kMaxGroups = 64;  // pipeline groups of one dmuon_muon_step_host call
+// dmuon_muon_step_host gathers with one launch instead of a copy per matrix from this many matrices on,
+// when they average less than this many gradient bytes.
+constexpr int kGatherMinCount = 64;
+constexpr int64_t kGatherMaxAvgBytes = int64_t(4) << 20;
 
 int64_t round_up(int64_t v, int64_t a) { return (v + a - 1) / a * a; }
 
@@ -178,6 +182,13 @@ struct DeviceState {
   cudaStream_t copy_stream = nullptr;
   cudaEvent_t entry = nullptr;
   std::vector<cudaEvent_t> copied, read;
+  // Gather table of the last host-gradient call that took the one-launch gather (many small matrices):
+  // built for gather_key (host pointers, device pointers, sizes), kept on the device.
+  std::vector<uintptr_t> gather_key;
+  bool gather_ok = false;  // every host pointer of gather_key is device-accessible
+  char* gather_buf = nullptr;
+  size_t gather_bytes = 0;
+  int64_t gather_chunks = 0;
 };
 
 std::mutex g_mu;
@@ -910,6 +921,91 @@ int ensure_pipeline(DeviceState& ds, size_t n) {
 
 int check_matrix_list(int count, const int64_t* rows, const int64_t* cols);
 
+// The device gather table for these host -> device copies (built once per set of pointers and sizes).
+// Leaves ds.gather_ok false when some host pointer is not readable by the device (pageable memory on a
+// device without host page-table access): the caller then copies with the copy engines.
+int ensure_gather(DeviceState& ds, int count, const void* const* src, void* const* dst, const int64_t* bytes,
+                  cudaStream_t stream) {
+  std::vector<uintptr_t> key;
+  key.reserve(3 * static_cast<size_t>(count));
+  for (int i = 0; i < count; ++i) {
+    key.push_back(reinterpret_cast<uintptr_t>(src[i]));
+    key.push_back(reinterpret_cast<uintptr_t>(dst[i]));
+    key.push_back(static_cast<uintptr_t>(bytes[i]));
+  }
+  int dev = 0, pageable = 0;
+  DM_CUDA(cudaGetDevice(&dev), "cudaGetDevice");
+  if (cudaDeviceGetAttribute(&pageable, cudaDevAttrPageableMemoryAccess, dev) != cudaSuccess) {
+    cudaGetLastError();
+    pageable = 0;
+  }
+  // The device address of host pointer i, or null when the device cannot read it.
+  auto resolve = [&](int i) -> const void* {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, src[i]) != cudaSuccess) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    if (a.type == cudaMemoryTypeHost && a.devicePointer) return a.devicePointer;  // page-locked, mapped
+    if (a.type == cudaMemoryTypeUnregistered && pageable) return src[i];          // through host page tables
+    return nullptr;
+  };
+  if (key == ds.gather_key) {
+    // With host page-table access every host address stays readable; without it the same addresses may
+    // have been unpinned since the table was built, so they are checked again.
+    if (ds.gather_ok && !pageable) {
+      for (int i = 0; i < count; ++i)
+        if (!resolve(i)) {
+          ds.gather_key.clear();
+          ds.gather_ok = false;
+          return DMUON_OK;
+        }
+    }
+    return DMUON_OK;
+  }
+  ds.gather_key.clear();
+  ds.gather_ok = false;
+  std::vector<GatherItem> items(count);
+  std::vector<int64_t> prefix(count + 1, 0);
+  for (int i = 0; i < count; ++i) {
+    const void* s = resolve(i);
+    if (!s) {
+      ds.gather_key = key;  // remember the verdict for this pointer set
+      return DMUON_OK;
+    }
+    items[i] = GatherItem{s, dst[i], bytes[i]};
+    prefix[i + 1] = prefix[i] + (bytes[i] + kGatherChunk - 1) / kGatherChunk;
+  }
+  if (prefix[count] >= (int64_t(1) << 31)) return fail(DMUON_ERR_UNSUPPORTED, "too many gradient bytes for one gather");
+  const size_t need = sizeof(GatherItem) * count + 256 + sizeof(int64_t) * (count + 1);
+  // An earlier call, possibly on another stream, may still be reading the old table.
+  if (ds.gather_buf) DM_CUDA(cudaDeviceSynchronize(), "cudaDeviceSynchronize before replacing the gather table");
+  if (need > ds.gather_bytes) {
+    if (ds.gather_buf) {
+      cudaFree(ds.gather_buf);
+      ds.gather_buf = nullptr;
+      ds.gather_bytes = 0;
+    }
+    if (cudaMalloc(&ds.gather_buf, need) != cudaSuccess) {
+      cudaGetLastError();
+      ds.gather_buf = nullptr;
+      return fail(DMUON_ERR_OOM, "cudaMalloc of the %zu-byte gather table failed", need);
+    }
+    ds.gather_bytes = need;
+  }
+  const size_t off_prefix = (sizeof(GatherItem) * count + 255) / 256 * 256;
+  DM_CUDA(cudaMemcpyAsync(ds.gather_buf, items.data(), sizeof(GatherItem) * count, cudaMemcpyHostToDevice, stream),
+          "upload gather items");
+  DM_CUDA(cudaMemcpyAsync(ds.gather_buf + off_prefix, prefix.data(), sizeof(int64_t) * (count + 1),
+                          cudaMemcpyHostToDevice, stream),
+          "upload gather prefix");
+  DM_CUDA(cudaStreamSynchronize(stream), "cudaStreamSynchronize after the gather table upload");
+  ds.gather_chunks = prefix[count];
+  ds.gather_key = key;
+  ds.gather_ok = true;
+  return DMUON_OK;
+}
+
 // Validation and key of dmuon_muon_step (shared with dmuon_muon_step_host).
 int muon_key(int count, float* const* params, const void* const* grads, int grad_dtype, float* const* momenta,
              const int64_t* rows, const int64_t* cols, float* norms_out, float lr, float beta, const float* coeffs,
@@ -1068,12 +1164,37 @@ int dmuon_muon_step_host(int count, float* const* params, const void* const* gra
       const int64_t per_group = int64_t(3) << 30;
       groups = static_cast<int>(std::min<int64_t>(8, std::max<int64_t>(1, (bytes + per_group - 1) / per_group)));
     }
-    key.groups = groups;
     cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
     std::lock_guard<std::mutex> lock(g_mu);
     DeviceState* ds = nullptr;
     st = current_device(&ds);
     if (st != DMUON_OK) return st;
+    // Many small matrices (here a copy-engine call per matrix costs more host time than its transfer):
+    // one gather launch on cuda_stream reads every gradient out of host memory, then the step runs as
+    // one group. Needs device-readable host memory; otherwise the copy engines below.
+    {
+      int64_t total = 0;
+      for (int i = 0; i < count; ++i) total += rows[i] * cols[i] * static_cast<int64_t>(esize);
+      if (count >= kGatherMinCount && total < static_cast<int64_t>(count) * kGatherMaxAvgBytes) {
+        std::vector<int64_t> nbytes(count);
+        for (int i = 0; i < count; ++i) nbytes[i] = rows[i] * cols[i] * static_cast<int64_t>(esize);
+        st = ensure_gather(*ds, count, grads_host, grads, nbytes.data(), stream);
+        if (st != DMUON_OK) return st;
+        if (ds->gather_ok) {
+          key.groups = 1;
+          std::vector<void*> xo(count, nullptr);
+          st = ensure_plan(*ds, key, G, Mo, W, xo, stream);
+          if (st != DMUON_OK) return st;
+          const size_t off_prefix = (sizeof(GatherItem) * count + 255) / 256 * 256;
+          DM_CUDA(launch_h2d_gather(reinterpret_cast<const GatherItem*>(ds->gather_buf),
+                                    reinterpret_cast<const int64_t*>(ds->gather_buf + off_prefix), count,
+                                    ds->gather_chunks, stream),
+                  "gradient gather launch");
+          return run_plan(*ds, ds->plan, coeffs, lr, beta, eps, norms_out, stream);
+        }
+      }
+    }
+    key.groups = groups;
     const size_t prev_groups = ds->copied.size();
     bool rebuilt = false;
     std::vector<void*> xo(count, nullptr);
@@ -1440,6 +1561,14 @@ int dmuon_release_workspace(void) {
     DM_CUDA(cudaFree(ds.adam.buf), "cudaFree(AdamW table)");
   }
   ds.adam = AdamPlan();
+  if (ds.gather_buf) {
+    DM_CUDA(cudaDeviceSynchronize(), "cudaDeviceSynchronize");
+    DM_CUDA(cudaFree(ds.gather_buf), "cudaFree(gather table)");
+  }
+  ds.gather_buf = nullptr;
+  ds.gather_bytes = 0;
+  ds.gather_key.clear();
+  ds.gather_ok = false;
   return DMUON_OK;
 }
 

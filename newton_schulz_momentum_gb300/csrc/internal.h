@@ -235,6 +235,19 @@ struct TpReduceLaunch {
 cudaError_t launch_shard_sumsq(const ShardSumsqLaunch& p, cudaStream_t stream);
 cudaError_t launch_tp_reduce(const TpReduceLaunch& p, cudaStream_t stream);
 
+// Host -> device gather of many small buffers in one launch (dmuon_muon_step_host with many small
+// matrices, where one copy-engine call per matrix would leave the host issuing copies): item i copies
+// bytes[i] from src[i], a device-accessible address of host memory, to dst[i]. Items are split into
+// kGatherChunk-byte chunks numbered by `prefix` (n + 1 entries).
+struct GatherItem {
+  const void* src;
+  void* dst;
+  int64_t bytes;
+};
+constexpr int64_t kGatherChunk = 65536;
+cudaError_t launch_h2d_gather(const GatherItem* items, const int64_t* prefix, int n, int64_t nchunks,
+                              cudaStream_t stream);
+
 // Diagnostic: one bounded wait on an mbarrier phase that nothing completes (records kDevTimeout).
 cudaError_t launch_selftest_wait(unsigned* status, unsigned long long limit_ns, cudaStream_t stream);
 cudaError_t launch_momentum_sumsq(const RowLaunch& p, int64_t nchunks, cudaStream_t stream);

@@ -401,8 +401,39 @@ __global__ void __launch_bounds__(kThreads) tp_reduce_kernel(const TpReduceLaunc
   }
 }
 
+// One 64 KB chunk of one gather item per CTA. With both addresses 16-byte aligned each thread issues
+// four 16-byte host loads before their stores (16 KB in flight per CTA and round, four rounds per
+// chunk) to cover the host link's latency; the unaligned remainder goes byte by byte.
+__global__ void __launch_bounds__(kThreads) h2d_gather_kernel(const GatherItem* items, const int64_t* prefix, int n) {
+  static_assert(kGatherChunk % (int64_t(kThreads) * 16 * 4) == 0, "a chunk is whole rounds of four 16-byte loads");
+  const int64_t chunk = blockIdx.x;
+  const int i = find_matrix(prefix, n, chunk);
+  const GatherItem it = items[i];
+  const int64_t begin = (chunk - prefix[i]) * kGatherChunk;
+  const int64_t end = min(begin + kGatherChunk, it.bytes);
+  const uint8_t* __restrict__ src = static_cast<const uint8_t*>(it.src);
+  uint8_t* __restrict__ dst = static_cast<uint8_t*>(it.dst);
+  int64_t from = begin;
+  if (((reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(dst)) & 15) == 0) {
+    const int64_t vend = begin + ((end - begin) & ~int64_t(15));
+    constexpr int64_t kStride = int64_t(kThreads) * 16;
+    for (int64_t b0 = begin + threadIdx.x * 16; b0 < vend; b0 += 4 * kStride) {
+      uint4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (b0 + u * kStride < vend) v[u] = __ldcs(reinterpret_cast<const uint4*>(src + b0 + u * kStride));
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (b0 + u * kStride < vend) *reinterpret_cast<uint4*>(dst + b0 + u * kStride) = v[u];
+    }
+    from = vend;
+  }
+  for (int64_t b = from + threadIdx.x; b < end; b += kThreads) dst[b] = src[b];
+}
+
 // One thread waits, through the same bounded wait the library's kernels use, on an mbarrier phase that
 // nothing completes: after limit_ns it gives up and records kDevTimeout in the status word.
+
 __global__ void selftest_wait_kernel(unsigned* status, unsigned long long limit_ns) {
   __shared__ uint64_t bar;
   __shared__ int abort_flag;
@@ -424,6 +455,13 @@ cudaError_t launch_shard_sumsq(const ShardSumsqLaunch& p, cudaStream_t stream) {
 
 cudaError_t launch_tp_reduce(const TpReduceLaunch& p, cudaStream_t stream) {
   tp_reduce_kernel<<<static_cast<unsigned>(p.m), kThreads, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_h2d_gather(const GatherItem* items, const int64_t* prefix, int n, int64_t nchunks,
+                              cudaStream_t stream) {
+  if (nchunks <= 0) return cudaSuccess;
+  h2d_gather_kernel<<<static_cast<unsigned>(nchunks), kThreads, 0, stream>>>(items, prefix, n);
   return cudaGetLastError();
 }
 

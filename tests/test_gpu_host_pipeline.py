@@ -135,3 +135,17 @@ def test_pipelined_against_oracle(dm):
         assert abs(float(norms_out[0][i]) - ref["norm"]) <= 1e-5 * ref["norm"]
         upd = (W0[i].astype(np.float64) - W[i].numpy().astype(np.float64)) / 0.02
         assert np.linalg.norm(upd - ref["O"]) <= 2e-2 * np.linalg.norm(ref["O"])
+
+
+# Many small matrices take the one-launch gather out of host memory instead of a copy per matrix.
+MANY_SMALL = [(96, 200), (200, 96), (64, 64), (128, 512), (7, 1), (33, 130)] * 12   # fused small-matrix plan
+MANY_MEDIUM = [(300, 264), (264, 520), (256, 256)] * 24                           # grouped GEMM plan
+
+
+@pytest.mark.parametrize("pinned", [True, False])
+@pytest.mark.parametrize("shapes", [MANY_SMALL, MANY_MEDIUM], ids=["fused", "grouped"])
+def test_many_small_matrices_gather(dm, shapes, pinned):
+    steps = [_grads(shapes, 1300, torch.float32), _grads(shapes, 1400, torch.float32)]
+    ref = _reference(dm, shapes, steps, torch.float32)
+    got = _pipelined(dm, shapes, steps, torch.float32, 0, pinned=pinned)
+    assert _equal(ref, got)
