@@ -10,12 +10,18 @@
 // the m x m products (R R, Z Q, Z R, S Z) read their right factor MN-major, with no assumption that it is
 // symmetric; Q X reads X MN-major. Accumulators live in tensor memory (up to 512 fp32 columns).
 //
-// Each phase: one thread issues the MMAs and commits to an mbarrier; all four warps wait, read their
-// 32 accumulator rows with tcgen05.ld, apply the step's fp32 recipe and write the fp16 result back into
-// shared memory (in place where the recipe reads the old value: each thread rewrites only its own row,
-// after the MMA that read it has completed). Rows and columns beyond the matrix are kept at zero. The
-// final Q X (or B X + a X) goes out as W += w_beta * O by TMA reduce-add (TMA store when W is
-// overwritten, direct stores when W rows are not 16-byte aligned). Every wait is bounded.
+// Each phase: one thread issues the MMAs and commits them to mbarriers; eight warps finish the phase, two
+// per tensor-memory lane quarter (32 rows), one for each half of the output columns. A warp reads its
+// accumulator columns with tcgen05.ld (two loads in flight per wait), applies the step's fp32 recipe and
+// writes the fp16 result back into shared memory (in place where the recipe reads the old value: a
+// thread rewrites only its own row's columns). The issuing thread, at about one MMA per 70 cycles, is the
+// limit of the small products, so X X^T and the m x m products are single N = 128 products (all warps
+// wait for all of it); the X-wide products (Q X, B X) go in two halves of output columns with a barrier
+// each, so the first half's epilogue overlaps the second half's MMAs -- safe in place, because each half
+// reads only its own column blocks of X. fp16 overflow is tracked with one packed FMA per pair of
+// values. Rows and columns beyond the matrix are kept at zero. The final Q X (or B X + a X) goes out as
+// W += w_beta * O by TMA reduce-add (TMA store when W is overwritten, direct stores when W rows are not
+// 16-byte aligned); in the Gram form the next matrix's X is fetched under it. Every wait is bounded.
 #include <algorithm>
 
 #include "internal.h"
@@ -33,6 +39,7 @@ constexpr int kZOff = 10 * kBlk;  // Z; the weight-update staging area at the en
 constexpr int kQOff = 12 * kBlk;  // Q
 constexpr int kOpBytes = 14 * kBlk;
 constexpr int kSmallSmem = kOpBytes + 256 + 1024;
+constexpr int kSmallThreads = 256;  // 8 warps: two per tensor-memory lane quarter, one per column half
 static_assert(kSmallSmem <= 232448, "shared memory budget");
 
 // Byte offset of element (r, c) in an operand buffer.
@@ -40,26 +47,43 @@ __device__ __forceinline__ uint32_t op_off(int r, int c) {
   return static_cast<uint32_t>((c >> 6) * kBlk + r * 128 + ((((c & 63) >> 3) ^ (r & 7)) << 4) + ((c & 7) << 1));
 }
 
-__device__ __forceinline__ void load_row32(const uint8_t* buf, int r, int c0, float (&e)[32]) {
+// 8 consecutive fp16 columns [c0, c0 + 8) of row r of an operand buffer (c0 a multiple of 8), as fp32.
+__device__ __forceinline__ void load8(const uint8_t* buf, int r, int c0, float (&e)[8]) {
+  const uint4 x = *reinterpret_cast<const uint4*>(buf + op_off(r, c0));
+  const __half2* h = reinterpret_cast<const __half2*>(&x);
 #pragma unroll
-  for (int u = 0; u < 4; ++u) {
-    const uint4 x = *reinterpret_cast<const uint4*>(buf + op_off(r, c0 + 8 * u));
-    const __half2* h = reinterpret_cast<const __half2*>(&x);
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const float2 f = __half22float2(h[k]);
-      e[8 * u + 2 * k] = f.x;
-      e[8 * u + 2 * k + 1] = f.y;
-    }
+  for (int k = 0; k < 4; ++k) {
+    const float2 f = __half22float2(h[k]);
+    e[2 * k] = f.x;
+    e[2 * k + 1] = f.y;
   }
 }
 
-__device__ __forceinline__ void store_row32(uint8_t* buf, int r, int c0, const float (&v)[32]) {
+// v rounded to fp16 as row r, columns [c0, c0 + 64). chk turns NaN if a value rounded to an infinity or
+// was NaN (h * 0 + chk: one packed FMA per pair instead of a test per value).
+__device__ __forceinline__ void store_row64(uint8_t* buf, int r, int c0, const float (&v)[64], __half2& chk) {
+  const __half2 zero2 = __float2half2_rn(0.f);
 #pragma unroll
-  for (int u = 0; u < 4; ++u)
-    *reinterpret_cast<uint4*>(buf + op_off(r, c0 + 8 * u)) =
-        make_uint4(pack_half2(v[8 * u + 0], v[8 * u + 1]), pack_half2(v[8 * u + 2], v[8 * u + 3]),
-                   pack_half2(v[8 * u + 4], v[8 * u + 5]), pack_half2(v[8 * u + 6], v[8 * u + 7]));
+  for (int u = 0; u < 8; ++u) {
+    uint32_t w[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const __half2 h = __floats2half2_rn(v[8 * u + 2 * q], v[8 * u + 2 * q + 1]);
+      chk = __hfma2(h, zero2, chk);
+      w[q] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    *reinterpret_cast<uint4*>(buf + op_off(r, c0 + 8 * u)) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+// 64 consecutive fp32 accumulator columns of this thread's TMEM lane: both loads in flight, one wait.
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
+  uint32_t r[64];
+  tmem_ld32_issue(taddr, r);
+  tmem_ld32_issue(taddr + 32, r + 32);
+  tmem_ld_wait(r);
+#pragma unroll
+  for (int k = 0; k < 64; ++k) v[k] = __uint_as_float(r[k]);
 }
 
 // acc[0, N) (+)= A (128 x K, K-major at a) * B; B K-major (rows = output columns) or MN-major (rows = the
@@ -74,27 +98,32 @@ __device__ __forceinline__ void issue_product(uint32_t d_tmem, uint32_t a, uint3
   }
 }
 
-__global__ void __launch_bounds__(128, 1) ns_small_kernel(const __grid_constant__ SmallLaunch p) {
+__global__ void __launch_bounds__(kSmallThreads, 1) ns_small_kernel(const __grid_constant__ SmallLaunch p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bar_x = reinterpret_cast<uint64_t*>(smem + kOpBytes);
-  uint64_t* bar_mma = bar_x + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_mma + 1);
+  uint64_t* bar_mma = bar_x + 1;  // [0]: the products of output columns [0, split), [1]: all of them
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_mma + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  uint8_t* Xs = smem + kXOff;
-  uint8_t* Rs = smem + kROff;
-  uint8_t* Zs = smem + kZOff;
-  uint8_t* Qs = smem + kQOff;
-  const uint32_t sx = smem_u32(Xs), sr = smem_u32(Rs), sz = smem_u32(Zs), sq = smem_u32(Qs);
+  volatile int* x_issued = abort_flag + 1;  // X loads requested so far (one bar_x phase each)
+  uint8_t* const Xs = smem + kXOff;
+  uint8_t* const Rs = smem + kROff;  // R, and S while the R update runs
+  uint8_t* const Zs = smem + kZOff;  // Z; with R, the staging area of the weight update
+  uint8_t* const Qs = smem + kQOff;
+  const uint32_t sx = smem_u32(Xs), sq = smem_u32(Qs);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
-  const int row = tid;  // tensor-memory lane = output row
+  const int quarter = warp & 3;  // tensor-memory lanes 32 * quarter ... : the rows this warp owns
+  const int half = warp >> 2;    // which half of each product's output columns this warp finishes
+  const int row = quarter * 32 + lane;
 
   if (tid == 0) {
     mbar_init(bar_x, 1);
-    mbar_init(bar_mma, 1);
+    mbar_init(&bar_mma[0], 1);
+    mbar_init(&bar_mma[1], 1);
     *abort_flag = 0;
+    *x_issued = 0;
     fence_barrier_init();
   }
   if (warp == 0) tmem_alloc(tmem_slot, 512);
@@ -102,163 +131,264 @@ __global__ void __launch_bounds__(128, 1) ns_small_kernel(const __grid_constant_
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t my_tmem = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+  const uint32_t my_tmem = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
 
   uint32_t x_phase = 0, mma_phase = 0;
   bool bad = false;
+  __half2 chk16 = __float2half2_rn(0.f);  // NaN once an fp16 operand overflowed
+  float chk32 = 0.f;                      // NaN once an fp32 output was not finite
 
-  // Issue (one thread) and wait for (everyone) one phase's products; smem operands must be fenced and
-  // synchronised by the caller. Returns false (uniformly) if a wait gave up.
-  auto mma_phase_done = [&]() -> bool {
-    bool ok = wait_bounded(bar_mma, mma_phase, abort_flag, p.status, kWaitLimitNs, true);
+  // One thread: request job jj's X (rows >= m and columns >= n arrive as zeros). Every earlier read of X,
+  // by the tensor core or by threads, has completed and been synchronised.
+  auto issue_x = [&](int jj) {
+    const SmallJob& nj = p.jobs[jj];
+    const int nbj = (nj.n + 63) / 64;
+    fence_async_smem();
+    mbar_arrive_expect_tx(bar_x, static_cast<uint32_t>(nbj * kBlk));
+    for (int c = 0; c < nbj; ++c) tma_load_2d(sx + c * kBlk, &nj.tmX, c * 64, 0, bar_x);
+    *x_issued = *x_issued + 1;
+  };
+  // Wait for this warp's half of the phase's products, or for all of them (the second barrier is
+  // committed after both halves).
+  auto wait_half = [&](bool all = false) -> bool {
+    const bool ok = wait_bounded(&bar_mma[all ? 1 : half], mma_phase, abort_flag, p.status, kWaitLimitNs, true);
     mma_phase ^= 1u;
-    ok = __syncthreads_and(ok) != 0;
     tc_fence_after();
     return ok;
   };
-  // Make this phase's shared-memory writes visible to the tensor cores and release tensor memory.
-  auto operands_ready = [&]() {
+  // End of a phase: shared-memory results visible to the tensor core, tensor-memory reads done, every
+  // thread here. False (uniformly) if some wait gave up.
+  auto phase_end = [&](bool ok) -> bool {
     fence_async_smem();
     tc_fence_before();
-    __syncthreads();
+    return __syncthreads_and(ok) != 0;
   };
 
-  for (int j = blockIdx.x; j < p.njobs; j += gridDim.x) {
+  int iter = 0;
+  for (int j = blockIdx.x; j < p.njobs; j += gridDim.x, ++iter) {
     const SmallJob& job = p.jobs[j];
     const int m = job.m, n = job.n;
     const int nb = (n + 63) / 64;  // column blocks of X
     const int ncols = nb * 64;
+    const int split = ((nb + 1) >> 1) * 64;  // X-wide products: columns [0, split) then [split, ncols)
+    const int c_lo = half ? split : 0, c_hi = half ? ncols : split;
+    const int c_mm = 64 * half;  // m x m products: this warp's 64 columns
+    const bool has_next = j + static_cast<int>(gridDim.x) < p.njobs;
 
-    // ---- X into shared memory (rows >= m and columns >= n arrive as zeros)
-    if (tid == 0) {
-      fence_async_smem();  // the previous matrix's reads of X precede this overwrite
-      mbar_arrive_expect_tx(bar_x, static_cast<uint32_t>(nb * kBlk));
-      for (int c = 0; c < nb; ++c) tma_load_2d(sx + c * kBlk, &job.tmX, c * 64, 0, bar_x);
-    }
+    if (tid == 0 && *x_issued == iter) issue_x(j);  // not prefetched during the previous matrix
     bool ok = wait_bounded(bar_x, x_phase, abort_flag, p.status, kWaitLimitNs, true);
     x_phase ^= 1u;
     if (!__syncthreads_and(ok)) break;
 
+    // Products, issued by one thread. R = X X^T and the m x m products are one N = 128 product each,
+    // committed to both barriers: the issuing thread is the limit, so fewer, wider MMAs win over an
+    // early start for half of the columns.
+    auto issue_gram = [&]() {
+      tc_fence_after();
+      issue_product(tmem, sx, sx, ncols, 128, false);
+      mma_commit(&bar_mma[0]);
+      mma_commit(&bar_mma[1]);
+    };
+    // acc = A * B for m x m operands, B MN-major.
+    auto issue_mm = [&](uint32_t a, uint32_t b) {
+      tc_fence_after();
+      issue_product(tmem, a, b, 128, 128, true);
+      mma_commit(&bar_mma[0]);
+      mma_commit(&bar_mma[1]);
+    };
+    // acc[0, ncols) = A (128 x 128 at a) * X (MN-major), in two halves of output columns, each committed
+    // to its own barrier (N up to 256 per half).
+    auto issue_times_x = [&](uint32_t a) {
+      tc_fence_after();
+      issue_product(tmem, a, sx, 128, split, true);
+      mma_commit(&bar_mma[0]);
+      if (ncols > split)
+        issue_product(tmem + static_cast<uint32_t>(split), a, sx + (split / 64) * kBlk, 128, ncols - split, true);
+      mma_commit(&bar_mma[1]);
+    };
+
     // R = X X^T, written to Rs (zero outside m x m).
     auto gram_of_x = [&]() -> bool {
-      if (tid == 0) {
-        tc_fence_after();
-        issue_product(tmem, sx, sx, ncols, 128, false);
-        mma_commit(bar_mma);
-      }
-      if (!mma_phase_done()) return false;
-      for (int c = 0; c < 128; c += 32) {
-        float v[32];
-        tmem_ld32(my_tmem + c, v);
+      if (tid == 0) issue_gram();
+      bool good = wait_half();
+      if (good) {
+        float v[64];
+        tmem_ld64(my_tmem + c_mm, v);
+        if (m < 128) {
 #pragma unroll
-        for (int k = 0; k < 32; ++k)
-          if (row >= m || c + k >= m) v[k] = 0.f;
-#pragma unroll
-        for (int k = 0; k < 32; ++k) bad |= !fp16_ok(v[k]);
-        store_row32(Rs, row, c, v);
-      }
-      operands_ready();
-      return true;
-    };
-    // acc = A * B for an m x m pair (B MN-major), then out = s_acc * acc + s_e * E + s_i * [i == j]
-    // (E read from `e` before out is written; out may equal e or be a third buffer).
-    auto mm_phase = [&](uint32_t a, uint32_t b, uint8_t* e, uint8_t* out, float s_acc, float s_e, float s_i,
-                        uint8_t* out2, float s_i2) -> bool {
-      if (tid == 0) {
-        tc_fence_after();
-        issue_product(tmem, a, b, 128, 128, true);
-        mma_commit(bar_mma);
-      }
-      if (!mma_phase_done()) return false;
-      for (int c = 0; c < 128; c += 32) {
-        float v[32], ev[32];
-        tmem_ld32(my_tmem + c, v);
-        if (e) load_row32(e, row, c, ev);
-#pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          float x = s_acc * v[k] + (e ? s_e * ev[k] : 0.f);
-          if (c + k == row) x += s_i;
-          v[k] = (row >= m || c + k >= m) ? 0.f : x;
-          bad |= !fp16_ok(v[k]);
+          for (int k = 0; k < 64; ++k)
+            if (row >= m || c_mm + k >= m) v[k] = 0.f;
         }
-        store_row32(out, row, c, v);
-        if (out2) {
-#pragma unroll
-          for (int k = 0; k < 32; ++k)
-            if (c + k == row && row < m) v[k] += s_i2;
-#pragma unroll
-          for (int k = 0; k < 32; ++k) bad |= !fp16_ok(v[k]);
-          store_row32(out2, row, c, v);
-        }
+        store_row64(Rs, row, c_mm, v, chk16);
       }
-      operands_ready();
-      return true;
+      return phase_end(good);
     };
-    // acc[0, ncols) = A (128 x 128 at a) * X (MN-major).
-    auto times_x = [&](uint32_t a) {
-      if (tid == 0) {
-        tc_fence_after();
-        for (int h = 0; h * 256 < ncols; ++h)
-          issue_product(tmem + static_cast<uint32_t>(h * 256), a, sx + h * 4 * kBlk, 128, min(256, ncols - h * 256), true);
-        mma_commit(bar_mma);
-      }
-    };
-    // X = s_acc * acc + s_e * X over the first ncols columns (zero outside m x n), in place.
-    auto x_update = [&](float s_acc, float s_e) {
-      for (int c = 0; c < ncols; c += 32) {
-        float v[32], ev[32];
-        tmem_ld32(my_tmem + c, v);
-        if (s_e != 0.f) load_row32(Xs, row, c, ev);
+    // acc = A * B for an m x m pair (B MN-major), then out = s_acc * acc + s_e * E (E read from `e`; out
+    // may equal e, since every product of the phase is complete when a thread rewrites its own row's
+    // columns) and, when out2 is given, out2 = out + s_i2 I.
+    auto mm_phase = [&](uint8_t* a, uint8_t* b, uint8_t* e, uint8_t* out, float s_acc, float s_e, uint8_t* out2,
+                        float s_i2) -> bool {
+      if (tid == 0) issue_mm(smem_u32(a), smem_u32(b));
+      bool good = wait_half();
+      if (good) {
+        float v[64];
+        tmem_ld64(my_tmem + c_mm, v);
+        if (e) {
 #pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          const float x = s_acc * v[k] + (s_e != 0.f ? s_e * ev[k] : 0.f);
-          v[k] = (row >= m || c + k >= n) ? 0.f : x;
-          bad |= !fp16_ok(v[k]);
-        }
-        store_row32(Xs, row, c, v);
-      }
-      operands_ready();
-    };
-    // W += w_beta * (s_acc * acc + s_e * X) (or W = ...), W in the caller's orientation.
-    auto w_update = [&](float s_acc, float s_e) {
-      uint8_t* stage = Zs + warp * 4096;
-      const uint32_t sbuf = smem_u32(stage);
-      const int row0 = warp * 32;
-      const bool tma_w = job.tma_w && (p.w_alpha == 0.f || p.w_alpha == 1.f);
-      if (row0 < m) {
-        for (int c = 0; c < ncols && c < n; c += 32) {
-          float v[32], ev[32];
-          tmem_ld32(my_tmem + c, v);
-          if (s_e != 0.f) load_row32(Xs, row, c, ev);
+          for (int u = 0; u < 8; ++u) {
+            float ev[8];
+            load8(e, row, c_mm + 8 * u, ev);
 #pragma unroll
-          for (int k = 0; k < 32; ++k) {
-            const float x = s_acc * v[k] + (s_e != 0.f ? s_e * ev[k] : 0.f);
-            v[k] = (row >= m || c + k >= n) ? 0.f : x;
-            bad |= !isfinite(v[k]);
+            for (int k = 0; k < 8; ++k) v[8 * u + k] = s_acc * v[8 * u + k] + s_e * ev[k];
           }
+        } else {
+#pragma unroll
+          for (int k = 0; k < 64; ++k) v[k] *= s_acc;
+        }
+        if (m < 128) {
+#pragma unroll
+          for (int k = 0; k < 64; ++k)
+            if (row >= m || c_mm + k >= m) v[k] = 0.f;
+        }
+        store_row64(out, row, c_mm, v, chk16);
+        if (out2) {
+          if (row < m && row >= c_mm && row < c_mm + 64) {
+#pragma unroll
+            for (int k = 0; k < 64; ++k)
+              if (c_mm + k == row) v[k] += s_i2;
+          }
+          store_row64(out2, row, c_mm, v, chk16);
+        }
+      }
+      return phase_end(good);
+    };
+    // Q = Z Q + a Q and S = Z R + a R together (both need only Z): one wait and one epilogue for two
+    // products, in tensor-memory columns [0, 128) and [128, 256).
+    auto zq_zr_phase = [&](float a) -> bool {
+      if (tid == 0) {
+        tc_fence_after();
+        issue_product(tmem, smem_u32(Zs), smem_u32(Qs), 128, 128, true);
+        issue_product(tmem + 128, smem_u32(Zs), smem_u32(Rs), 128, 128, true);
+        mma_commit(&bar_mma[0]);
+        mma_commit(&bar_mma[1]);
+      }
+      bool good = wait_half();
+      if (good) {
+#pragma unroll 1
+        for (int t = 0; t < 2; ++t) {
+          uint8_t* o = t ? Rs : Qs;
+          float v[64];
+          tmem_ld64(my_tmem + 128 * t + c_mm, v);
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            float ev[8];
+            load8(o, row, c_mm + 8 * u, ev);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) v[8 * u + k] = v[8 * u + k] + a * ev[k];
+          }
+          if (m < 128) {
+#pragma unroll
+            for (int k = 0; k < 64; ++k)
+              if (row >= m || c_mm + k >= m) v[k] = 0.f;
+          }
+          store_row64(o, row, c_mm, v, chk16);
+        }
+      }
+      return phase_end(good);
+    };
+    // X = s_acc * acc + s_e * X over this warp's columns (zero outside m x n), in place: the other half's
+    // products read only the other half's column blocks of X.
+    auto x_update = [&](float s_acc, float s_e) -> bool {
+      bool good = wait_half();
+      if (good) {
+        for (int c = c_lo; c < c_hi; c += 64) {
+          float v[64];
+          tmem_ld64(my_tmem + c, v);
+          if (s_e != 0.f) {
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              float ev[8];
+              load8(Xs, row, c + 8 * u, ev);
+#pragma unroll
+              for (int k = 0; k < 8; ++k) v[8 * u + k] = s_acc * v[8 * u + k] + s_e * ev[k];
+            }
+          } else {
+#pragma unroll
+            for (int k = 0; k < 64; ++k) v[k] *= s_acc;
+          }
+          if (row >= m || c + 64 > n) {
+#pragma unroll
+            for (int k = 0; k < 64; ++k)
+              if (row >= m || c + k >= n) v[k] = 0.f;
+          }
+          store_row64(Xs, row, c, v, chk16);
+        }
+      }
+      return phase_end(good);
+    };
+    // W += w_beta * (s_acc * acc + s_e * X) (or W = ...), W in the caller's orientation. The R and Z
+    // buffers (64 KB, free by now) stage two 32 x 32 fp32 tiles per warp for the TMA reduce-adds. (The
+    // TMA unit moves about 20 bytes per cycle here whatever the box: 32 x 128 boxes filled by four warps
+    // together were slower, having fewer boxes in flight.)
+    auto w_update = [&](float s_acc, float s_e, bool good) -> bool {
+      uint8_t* stage = smem + kROff + warp * 8192;
+      const uint32_t sbuf = smem_u32(stage);
+      const int row0 = quarter * 32;
+      const bool tma_w = job.tma_w && (p.w_alpha == 0.f || p.w_alpha == 1.f);
+      if (good && row0 < m) {
+        for (int c = c_lo; c < c_hi && c < n; c += 64) {
+          float v[64];
+          tmem_ld64(my_tmem + c, v);
+          if (s_e != 0.f) {
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              float ev[8];
+              load8(Xs, row, c + 8 * u, ev);
+#pragma unroll
+              for (int k = 0; k < 8; ++k) v[8 * u + k] = s_acc * v[8 * u + k] + s_e * ev[k];
+            }
+          } else {
+#pragma unroll
+            for (int k = 0; k < 64; ++k) v[k] *= s_acc;
+          }
+          if (row >= m || c + 64 > n) {
+#pragma unroll
+            for (int k = 0; k < 64; ++k)
+              if (row >= m || c + k >= n) v[k] = 0.f;
+          }
+#pragma unroll
+          for (int k = 0; k < 64; ++k) chk32 = fmaf(v[k], 0.f, chk32);
           if (tma_w) {
-            if (lane == 0) bulk_wait_read0();
+            if (lane == 0) bulk_wait_read0();  // the previous group's tiles have left the staging area
             __syncwarp();
-            if (!job.trans) {
 #pragma unroll
-              for (int q = 0; q < 8; ++q)
-                *reinterpret_cast<float4*>(stage + sw128_f(lane, 4 * q)) =
-                    make_float4(p.w_beta * v[4 * q], p.w_beta * v[4 * q + 1], p.w_beta * v[4 * q + 2], p.w_beta * v[4 * q + 3]);
-            } else {
+            for (int t = 0; t < 2; ++t) {
+              uint8_t* tile = stage + t * 4096;
+              if (!job.trans) {
 #pragma unroll
-              for (int k = 0; k < 32; ++k) *reinterpret_cast<float*>(stage + sw128_f(k, lane)) = p.w_beta * v[k];
+                for (int q = 0; q < 8; ++q)
+                  *reinterpret_cast<float4*>(tile + sw128_f(lane, 4 * q)) =
+                      make_float4(p.w_beta * v[32 * t + 4 * q], p.w_beta * v[32 * t + 4 * q + 1],
+                                  p.w_beta * v[32 * t + 4 * q + 2], p.w_beta * v[32 * t + 4 * q + 3]);
+              } else {
+#pragma unroll
+                for (int k = 0; k < 32; ++k) *reinterpret_cast<float*>(tile + sw128_f(k, lane)) = p.w_beta * v[32 * t + k];
+              }
             }
             fence_async_smem();
             __syncwarp();
             if (lane == 0) {
-              const int x = job.trans ? row0 : c, y = job.trans ? c : row0;
-              if (p.w_alpha == 0.f) tma_store_2d(&job.tmW, sbuf, x, y);
-              else tma_reduce_add_2d(&job.tmW, sbuf, x, y);
+              for (int t = 0; t < 2 && c + 32 * t < n; ++t) {
+                const int cc = c + 32 * t;
+                const int x = job.trans ? row0 : cc, y = job.trans ? cc : row0;
+                if (p.w_alpha == 0.f) tma_store_2d(&job.tmW, sbuf + t * 4096, x, y);
+                else tma_reduce_add_2d(&job.tmW, sbuf + t * 4096, x, y);
+              }
               bulk_commit();
             }
           } else if (row < m) {
 #pragma unroll
-            for (int k = 0; k < 32; ++k) {
+            for (int k = 0; k < 64; ++k) {
               if (c + k < n) {
                 float* w = job.trans ? job.W + static_cast<int64_t>(c + k) * job.ldw + row
                                      : job.W + static_cast<int64_t>(row) * job.ldw + c + k;
@@ -268,9 +398,8 @@ __global__ void __launch_bounds__(128, 1) ns_small_kernel(const __grid_constant_
           }
         }
       }
-      if (lane == 0) bulk_wait_read0();  // the staging area is Z: free it before the next matrix
-      tc_fence_before();
-      __syncthreads();
+      if (lane == 0) bulk_wait_read0();  // the staging area is R and Z: free it before the next matrix
+      return phase_end(good);
     };
 
     bool alive = true;
@@ -281,49 +410,57 @@ __global__ void __launch_bounds__(128, 1) ns_small_kernel(const __grid_constant_
       for (int k = 0; alive && k < p.steps; ++k) {
         const float a = p.coef[3 * k], b = p.coef[3 * k + 1], c = p.coef[3 * k + 2];
         if (k > 0 && ((p.restart_mask >> k) & 1u)) {
-          times_x(sq);  // X <- Q X
-          if (!mma_phase_done()) { alive = false; break; }
-          x_update(1.f, 0.f);
-          if (!gram_of_x()) { alive = false; break; }
+          if (tid == 0) issue_times_x(sq);  // X <- Q X
+          if (!x_update(1.f, 0.f) || !gram_of_x()) { alive = false; break; }
           fresh = true;
         }
         // Z = b R + c R^2 (and Q = Z + a I after a (re)start)
-        if (!mm_phase(sr, sr, Rs, Zs, c, b, 0.f, fresh ? Qs : nullptr, a)) { alive = false; break; }
-        if (!fresh && !mm_phase(sz, sq, Qs, Qs, 1.f, a, 0.f, nullptr, 0.f)) { alive = false; break; }  // Q = ZQ + aQ
+        if (!mm_phase(Rs, Rs, Rs, Zs, c, b, fresh ? Qs : nullptr, a)) { alive = false; break; }
         const bool update_r = k + 1 < p.steps && !((p.restart_mask >> (k + 1)) & 1u);
-        if (update_r) {
-          if (!mm_phase(sz, sr, Rs, Rs, 1.f, a, 0.f, nullptr, 0.f)) { alive = false; break; }  // S = ZR + aR
-          if (!mm_phase(sr, sz, Rs, Rs, 1.f, a, 0.f, nullptr, 0.f)) { alive = false; break; }  // R = SZ + aS
+        if (!fresh && update_r) {
+          if (!zq_zr_phase(a)) { alive = false; break; }  // Q = ZQ + aQ, S = ZR + aR
+        } else {
+          if (!fresh && !mm_phase(Zs, Qs, Qs, Qs, 1.f, a, nullptr, 0.f)) { alive = false; break; }  // Q = ZQ + aQ
+          if (update_r && !mm_phase(Zs, Rs, Rs, Rs, 1.f, a, nullptr, 0.f)) { alive = false; break; }  // S = ZR + aR
         }
+        if (update_r && !mm_phase(Rs, Zs, Rs, Rs, 1.f, a, nullptr, 0.f)) { alive = false; break; }  // R = SZ + aS
         fresh = false;
       }
       if (!alive) break;
-      times_x(sq);  // O = Q X
-      if (!mma_phase_done()) break;
-      w_update(1.f, 0.f);
+      if (tid == 0) issue_times_x(sq);  // O = Q X
+      const bool good = wait_half();
+      // The second barrier means every product of this matrix is done with X: fetch the next one now,
+      // under the weight update.
+      if (half == 1 && lane == 0 && quarter == 0 && good && has_next) issue_x(j + gridDim.x);
+      if (!w_update(1.f, 0.f, good)) break;
     } else {
       // ---- direct iteration
       for (int k = 0; alive && k < p.steps; ++k) {
         const float a = p.coef[3 * k], b = p.coef[3 * k + 1], c = p.coef[3 * k + 2];
         if (!gram_of_x()) { alive = false; break; }                                       // A = X X^T
-        if (!mm_phase(sr, sr, Rs, Zs, c, b, 0.f, nullptr, 0.f)) { alive = false; break; }  // B = b A + c A^2
-        times_x(sz);                                                                       // B X
-        if (!mma_phase_done()) { alive = false; break; }
-        if (k + 1 < p.steps) x_update(1.f, a);  // X = B X + a X
-        else w_update(1.f, a);
+        if (!mm_phase(Rs, Rs, Rs, Zs, c, b, nullptr, 0.f)) { alive = false; break; }  // B = b A + c A^2
+        if (tid == 0) issue_times_x(smem_u32(Zs));                                         // B X
+        if (k + 1 < p.steps) {
+          if (!x_update(1.f, a)) { alive = false; break; }  // X = B X + a X
+        } else if (!w_update(1.f, a, wait_half(true))) {  // Z, in the staging area, is read by both halves
+          alive = false;
+          break;
+        }
       }
       if (!alive) break;
     }
   }
 
   if (lane == 0) bulk_wait0();
+  bad |= __hisnan(__low2half(chk16)) || __hisnan(__high2half(chk16)) || chk32 != chk32;
   if (bad) atomicOr(p.status, kDevNonfinite);
   // After an abort, let any copy or MMA still in flight finish before shared and tensor memory go away.
   if (*abort_flag) {
     if (tid == 0) {
-      mma_commit(bar_mma);
-      wait_bounded(bar_mma, mma_phase, abort_flag, p.status, kDrainLimitNs, false);
-      wait_bounded(bar_x, x_phase ^ 1u, abort_flag, p.status, kDrainLimitNs, false);
+      mma_commit(&bar_mma[1]);
+      wait_bounded(&bar_mma[1], mma_phase, abort_flag, p.status, kDrainLimitNs, false);
+      const int issued = *x_issued;
+      if (issued > 0) wait_bounded(bar_x, static_cast<uint32_t>(issued - 1) & 1u, abort_flag, p.status, kDrainLimitNs, false);
     }
   }
   tc_fence_before();
@@ -360,7 +497,7 @@ cudaError_t launch_ns_small(const SmallLaunch& p, int sms, cudaStream_t stream) 
   if (p.njobs <= 0) return cudaSuccess;
   cudaError_t e = cudaFuncSetAttribute(ns_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmallSmem);
   if (e != cudaSuccess) return e;
-  ns_small_kernel<<<std::min(p.njobs, sms), 128, kSmallSmem, stream>>>(p);
+  ns_small_kernel<<<std::min(p.njobs, sms), kSmallThreads, kSmallSmem, stream>>>(p);
   return cudaGetLastError();
 }
 

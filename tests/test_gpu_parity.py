@@ -289,6 +289,29 @@ def test_small_fused_kernel_matches_oracle(dm, backend, restarts):
         assert check_update(W[i], Wd[i].cpu().numpy(), ref, 0.02) <= TOL_NS, (s, form)
 
 
+@pytest.mark.parametrize("backend,restarts", [("gram", (1, 3)), ("direct", ())])
+def test_small_fused_kernel_several_matrices_per_cta(dm, backend, restarts):
+    """More small matrices than CTAs (one per SM): each CTA runs two or three in turn, fetching the next
+    matrix's X while the current one's weight update drains (Gram) or after it (direct). A sample is
+    checked against the oracle; every matrix must be bit-identical to running it alone."""
+    shapes = (SMALL_SHAPES * 30)[:320]
+    W = [workloads.gaussian(s, 0.02, 2100 + i) for i, s in enumerate(shapes)]
+    G = [workloads.gaussian(s, 1.0, 2600 + i) for i, s in enumerate(shapes)]
+    Wd = [cuda(w) for w in W]
+    Md = [torch.zeros(s, dtype=torch.float32, device="cuda") for s in shapes]
+    dm.muon_step(Wd, [cuda(g) for g in G], Md, lr=0.02, beta=0.95, coeffs=dm.YOU, restarts=restarts,
+                 backend=backend)
+    dm.check_status()
+    for i in list(range(0, 320, 23)) + [151, 152, 303, 304, 319]:
+        ref = muon_ref(W[i], G[i], np.zeros(shapes[i]), 0.02, 0.95, ns64.YOU, restarts, backend)
+        assert check_update(W[i], Wd[i].cpu().numpy(), ref, 0.02) <= TOL_NS, (i, shapes[i])
+        alone_w = [cuda(W[i])]
+        dm.muon_step(alone_w, [cuda(G[i])], [torch.zeros(shapes[i], dtype=torch.float32, device="cuda")], lr=0.02,
+                     beta=0.95, coeffs=dm.YOU, restarts=restarts, backend=backend)
+        assert torch.equal(alone_w[0], Wd[i]), (i, shapes[i])
+    dm.check_status()
+
+
 def test_small_fused_ns_in_place(dm):
     for shape in ((128, 512), (512, 128), (1, 1), (96, 160)):
         for backend in ("gram", "direct"):
