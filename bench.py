@@ -438,8 +438,10 @@ def run_native(args):
     achieved = per_launch_flops / (gemm_ms / max(gemm_n, 1) * 1e-3) / 1e12 if gemm_ms > 0 else None
     launches = sum(n for _, n in kernel_times.values())
     rw_ms = sum(kernel_times[k][0] for k in ("momentum_sumsq", "finalize_norms", "normalize_cast"))
-    # momentum: G (2 B bf16 / 4 B fp32) + M read 4 + M write 4; normalise: M read 4 + X write 2
-    rw_bytes = (2 if gdtype == torch.bfloat16 else 4) + 4 + 4 + 4 + 2
+    # momentum: G (2 B bf16 / 4 B fp32) + M read 4 + M write 4; normalise: M read 4 + X write 2 (no
+    # separate normalise pass when the fused small-matrix kernel reads M itself)
+    fused_small = kernel_times["normalize_cast"][1] == 0
+    rw_bytes = (2 if gdtype == torch.bfloat16 else 4) + 4 + 4 + (0 if fused_small else 4 + 2)
 
     # dedicated ownership of this matrix set over 8 owner ranks (host-only LPT), timed and its balance
     layer_of = [int(name.split(".")[1]) if name.startswith("layers.") else 0 for name, _, _ in shapes]

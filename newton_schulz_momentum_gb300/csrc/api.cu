@@ -548,10 +548,7 @@ int build_plan_host(Plan& pl, const PlanKey& key, const std::vector<const void*>
     if (key.kind == kPlanMomNorm) continue;
     const size_t xbytes = sizeof(__half) * mi.m * mi.ldx;
     const size_t mbytes = sizeof(__half) * mi.m * mi.ldm;
-    if (pl.small_fused) {  // the fused kernel keeps every other operand on chip
-      mi.X = lay.take(xbytes);
-      continue;
-    }
+    if (pl.small_fused) continue;  // the fused kernel reads M itself and keeps every operand on chip
     mi.X = lay.take(xbytes);
     mi.Xb = lay.take(xbytes);
     mi.R = lay.take(mbytes);
@@ -743,8 +740,9 @@ int bind_plan(DeviceState& ds, Plan& pl, cudaStream_t stream) {
       const MatInfo& mi = pl.mats[i];
       std::memset(&pl.small_jobs[i], 0, sizeof(SmallJob));
       const char* err = nullptr;
-      if (!encode_small_job(pl.small_jobs[i], static_cast<const __half*>(at(mi.X)), mi.ldx, mi.W, mi.cols,
-                            static_cast<int>(mi.m), static_cast<int>(mi.n), mi.trans, mi.direct, &err))
+      const float* inv = reinterpret_cast<const float*>(base + pl.off_inv) + i;
+      if (!encode_small_job(pl.small_jobs[i], mi.M, mi.cols, inv, mi.W, mi.cols, static_cast<int>(mi.m),
+                            static_cast<int>(mi.n), mi.trans, mi.direct, &err))
         return fail(DMUON_ERR_CUDA, "%s", err);
     }
     DM_CUDA(cudaMemcpyAsync(base + pl.off_small, pl.small_jobs.data(), sizeof(SmallJob) * pl.small_jobs.size(),
@@ -825,7 +823,9 @@ int run_plan(DeviceState& ds, const Plan& pl, const float* coeffs, float lr, flo
     }
     if (group_read) DM_CUDA(cudaEventRecord(group_read[g], stream), "record a group's gradients as read");
     DM_CUDA(timed(1, stream, [&] { return launch_finalize_norms(rg, stream); }), "norm launch");
-    DM_CUDA(timed(2, stream, [&] { return launch_normalize_cast(rg, ncast, stream); }), "normalise/cast launch");
+    // The fused small-matrix kernel normalises and casts as it reads M.
+    if (!pl.small_fused)
+      DM_CUDA(timed(2, stream, [&] { return launch_normalize_cast(rg, ncast, stream); }), "normalise/cast launch");
     if (pl.small_fused) {
       SmallLaunch sl;
       std::memset(&sl, 0, sizeof(sl));

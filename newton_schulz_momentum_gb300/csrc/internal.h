@@ -117,12 +117,14 @@ constexpr int kSmallMaxM = 128;
 constexpr int kSmallMaxN = 512;
 
 struct alignas(128) SmallJob {
-  CUtensorMap tmX;  // X (fp16, m x n, ldx), box {64, 128}, 128-byte swizzle
   CUtensorMap tmW;  // W (fp32, caller orientation), box {32, 32}, 128-byte swizzle (when tma_w)
+  const float* M;   // momentum (fp32, caller orientation, leading dimension ldm): X = fp16(M * *inv)
+  const float* inv; // 1 / (||M||_F + eps), written by the norm pass
   float* W;
-  int64_t ldw;
+  int64_t ldm, ldw;
   int m, n;
-  int trans;   // W is stored transposed (the matrix was oriented)
+  int trans;   // M and W are stored transposed (the matrix was oriented)
+  int vec_m;   // M and its rows 16-byte aligned
   int tma_w;   // tmW valid; otherwise direct stores
   int direct;  // 1: direct iteration, 0: Gram iteration
 };
@@ -137,8 +139,8 @@ struct SmallLaunch {
   unsigned* status;
 };
 
-bool encode_small_job(SmallJob& job, const __half* X, int64_t ldx, float* W, int64_t ldw, int m, int n, bool trans,
-                      bool direct, const char** err);
+bool encode_small_job(SmallJob& job, const float* M, int64_t ldm, const float* inv, float* W, int64_t ldw, int m,
+                      int n, bool trans, bool direct, const char** err);
 cudaError_t launch_ns_small(const SmallLaunch& p, int sms, cudaStream_t stream);
 
 // ------------------------------------------------------------------------------------------------

@@ -76,6 +76,93 @@ __device__ __forceinline__ void store_row64(uint8_t* buf, int r, int c0, const f
   }
 }
 
+// X = fp16(M * inv) for X's column blocks [b_lo, b_hi) (zero outside m x n), done by `nth` threads (this one
+// is number th; nth is 128 or 256) in part `part` of `nparts` equal shares: the normalise-and-cast step of
+// the row-wise pass, done here so that X goes from M straight into shared memory. Every load is
+// coalesced and every index is a shift or an increment (the fill is bound by its own instructions):
+// M rows -- a warp takes X rows in turn, its lanes 8-column chunks of the row (two 16-byte loads each);
+// transposed (X rows are M columns) -- a warp takes (32-row slab, 8-column chunk) units, its lanes the
+// slab's rows (eight 4-byte loads each, one per M row). Batches of loads are in flight before any store.
+__device__ __forceinline__ void fill_x(uint8_t* Xs, const SmallJob& jb, int b_lo, int b_hi, int th, int nth, int part,
+                                       int nparts) {
+  if (b_hi <= b_lo) return;
+  const int jm = jb.m, jn = jb.n;
+  const float* const M = jb.M;
+  const int64_t ldm = jb.ldm;
+  const bool vec = jb.vec_m != 0;
+  const float inv = *jb.inv;
+  const int nw = nth >> 5, wid = th >> 5, ln = th & 31;
+  const int nch = 8 * (b_hi - b_lo);  // 8-column chunks in the range (8 ... 64)
+  if (!jb.trans) {
+    constexpr int kRows = 4;
+    const int rows_w = 128 / nw;  // rows per warp
+    const int i_lo = part * rows_w / nparts, i_hi = (part + 1) * rows_w / nparts;
+    for (int i0 = i_lo; i0 < i_hi; i0 += kRows) {
+      float4 v[kRows][2][2];
+#pragma unroll
+      for (int a = 0; a < kRows; ++a) {
+        const int r = wid + nw * (i0 + a);
+        const bool row_ok = i0 + a < i_hi && r < jm;
+        const float* rp = M + static_cast<int64_t>(r) * ldm;
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          const int c = 64 * b_lo + 8 * (ln + 32 * t);
+          v[a][t][0] = v[a][t][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (row_ok && ln + 32 * t < nch && c < jn) {
+            if (vec && c + 8 <= jn) {
+              v[a][t][0] = __ldcs(reinterpret_cast<const float4*>(rp + c));
+              v[a][t][1] = __ldcs(reinterpret_cast<const float4*>(rp + c + 4));
+            } else {
+              float e[8];
+#pragma unroll
+              for (int k = 0; k < 8; ++k) e[k] = c + k < jn ? rp[c + k] : 0.f;
+              v[a][t][0] = make_float4(e[0], e[1], e[2], e[3]);
+              v[a][t][1] = make_float4(e[4], e[5], e[6], e[7]);
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int a = 0; a < kRows; ++a) {
+        const int r = wid + nw * (i0 + a);
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          if (i0 + a >= i_hi || ln + 32 * t >= nch) continue;
+          const float4 x = v[a][t][0], y = v[a][t][1];
+          *reinterpret_cast<uint4*>(Xs + op_off(r, 64 * b_lo + 8 * (ln + 32 * t))) =
+              make_uint4(pack_half2(x.x * inv, x.y * inv), pack_half2(x.z * inv, x.w * inv),
+                         pack_half2(y.x * inv, y.y * inv), pack_half2(y.z * inv, y.w * inv));
+        }
+      }
+    }
+  } else {
+    constexpr int kUnits = 4;
+    const int units_w = 4 * nch / nw;  // (slab, chunk) units per warp: slab = unit & 3, chunk = unit >> 2
+    const int i_lo = part * units_w / nparts, i_hi = (part + 1) * units_w / nparts;
+    for (int i0 = i_lo; i0 < i_hi; i0 += kUnits) {
+      float v[kUnits][8];
+#pragma unroll
+      for (int a = 0; a < kUnits; ++a) {
+        const int k = wid + nw * (i0 + a);
+        const int r = 32 * (k & 3) + ln, c = 64 * b_lo + 8 * (k >> 2);
+        const bool live = i0 + a < i_hi && r < jm;
+        const float* cp = M + static_cast<int64_t>(c) * ldm + r;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[a][e] = live && c + e < jn ? __ldcs(cp + e * ldm) : 0.f;
+      }
+#pragma unroll
+      for (int a = 0; a < kUnits; ++a) {
+        if (i0 + a >= i_hi) continue;
+        const int k = wid + nw * (i0 + a);
+        const int r = 32 * (k & 3) + ln, c = 64 * b_lo + 8 * (k >> 2);
+        *reinterpret_cast<uint4*>(Xs + op_off(r, c)) =
+            make_uint4(pack_half2(v[a][0] * inv, v[a][1] * inv), pack_half2(v[a][2] * inv, v[a][3] * inv),
+                       pack_half2(v[a][4] * inv, v[a][5] * inv), pack_half2(v[a][6] * inv, v[a][7] * inv));
+      }
+    }
+  }
+}
+
 // 64 consecutive fp32 accumulator columns of this thread's TMEM lane: both loads in flight, one wait.
 __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
   uint32_t r[64];
@@ -101,11 +188,9 @@ __device__ __forceinline__ void issue_product(uint32_t d_tmem, uint32_t a, uint3
 __global__ void __launch_bounds__(kSmallThreads, 1) ns_small_kernel(const __grid_constant__ SmallLaunch p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* bar_x = reinterpret_cast<uint64_t*>(smem + kOpBytes);
-  uint64_t* bar_mma = bar_x + 1;  // [0]: the products of output columns [0, split), [1]: all of them
+  uint64_t* bar_mma = reinterpret_cast<uint64_t*>(smem + kOpBytes);  // [0]: output columns [0, split); [1]: all
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_mma + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  volatile int* x_issued = abort_flag + 1;  // X loads requested so far (one bar_x phase each)
   uint8_t* const Xs = smem + kXOff;
   uint8_t* const Rs = smem + kROff;  // R, and S while the R update runs
   uint8_t* const Zs = smem + kZOff;  // Z; with R, the staging area of the weight update
@@ -119,11 +204,9 @@ __global__ void __launch_bounds__(kSmallThreads, 1) ns_small_kernel(const __grid
   const int row = quarter * 32 + lane;
 
   if (tid == 0) {
-    mbar_init(bar_x, 1);
     mbar_init(&bar_mma[0], 1);
     mbar_init(&bar_mma[1], 1);
     *abort_flag = 0;
-    *x_issued = 0;
     fence_barrier_init();
   }
   if (warp == 0) tmem_alloc(tmem_slot, 512);
@@ -133,21 +216,11 @@ __global__ void __launch_bounds__(kSmallThreads, 1) ns_small_kernel(const __grid
   const uint32_t tmem = *tmem_slot;
   const uint32_t my_tmem = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
 
-  uint32_t x_phase = 0, mma_phase = 0;
+  uint32_t mma_phase = 0;
   bool bad = false;
   __half2 chk16 = __float2half2_rn(0.f);  // NaN once an fp16 operand overflowed
   float chk32 = 0.f;                      // NaN once an fp32 output was not finite
 
-  // One thread: request job jj's X (rows >= m and columns >= n arrive as zeros). Every earlier read of X,
-  // by the tensor core or by threads, has completed and been synchronised.
-  auto issue_x = [&](int jj) {
-    const SmallJob& nj = p.jobs[jj];
-    const int nbj = (nj.n + 63) / 64;
-    fence_async_smem();
-    mbar_arrive_expect_tx(bar_x, static_cast<uint32_t>(nbj * kBlk));
-    for (int c = 0; c < nbj; ++c) tma_load_2d(sx + c * kBlk, &nj.tmX, c * 64, 0, bar_x);
-    *x_issued = *x_issued + 1;
-  };
   // Wait for this warp's half of the phase's products, or for all of them (the second barrier is
   // committed after both halves).
   auto wait_half = [&](bool all = false) -> bool {
@@ -164,8 +237,8 @@ __global__ void __launch_bounds__(kSmallThreads, 1) ns_small_kernel(const __grid
     return __syncthreads_and(ok) != 0;
   };
 
-  int iter = 0;
-  for (int j = blockIdx.x; j < p.njobs; j += gridDim.x, ++iter) {
+  bool x_ready = false;  // X of the next matrix already in shared memory (filled under the weight update)
+  for (int j = blockIdx.x; j < p.njobs; j += gridDim.x) {
     const SmallJob& job = p.jobs[j];
     const int m = job.m, n = job.n;
     const int nb = (n + 63) / 64;  // column blocks of X
@@ -175,10 +248,21 @@ __global__ void __launch_bounds__(kSmallThreads, 1) ns_small_kernel(const __grid
     const int c_mm = 64 * half;  // m x m products: this warp's 64 columns
     const bool has_next = j + static_cast<int>(gridDim.x) < p.njobs;
 
-    if (tid == 0 && *x_issued == iter) issue_x(j);  // not prefetched during the previous matrix
-    bool ok = wait_bounded(bar_x, x_phase, abort_flag, p.status, kWaitLimitNs, true);
-    x_phase ^= 1u;
-    if (!__syncthreads_and(ok)) break;
+    if (!x_ready) {  // the first matrix, or one after a direct-form matrix: all threads fill X
+      fill_x(Xs, job, 0, nb, tid, kSmallThreads, 0, 1);
+      fence_async_smem();
+      __syncthreads();
+    }
+    x_ready = false;
+    const int nb_next = has_next ? (p.jobs[j + gridDim.x].n + 63) / 64 : 0;
+    // The next matrix's M is read at the end of this one, when every CTA is busy with memory at once;
+    // bring it into L2 now, under this matrix's products (M is contiguous: rows x ldm floats).
+    if (has_next && warp == 7) {
+      const SmallJob& nj = p.jobs[j + gridDim.x];
+      const int64_t bytes = static_cast<int64_t>(nj.trans ? nj.n : nj.m) * nj.ldm * 4 & ~int64_t(15);
+      for (int64_t off = static_cast<int64_t>(lane) * 16384; off < bytes; off += 32 * 16384)
+        bulk_prefetch_l2(reinterpret_cast<const char*>(nj.M) + off, static_cast<uint32_t>(bytes - off < 16384 ? bytes - off : 16384));
+    }
 
     // Products, issued by one thread. R = X X^T and the m x m products are one N = 128 product each,
     // committed to both barriers: the issuing thread is the limit, so fewer, wider MMAs win over an
@@ -330,11 +414,17 @@ __global__ void __launch_bounds__(kSmallThreads, 1) ns_small_kernel(const __grid
     // buffers (64 KB, free by now) stage two 32 x 32 fp32 tiles per warp for the TMA reduce-adds. (The
     // TMA unit moves about 20 bytes per cycle here whatever the box: 32 x 128 boxes filled by four warps
     // together were slower, having fewer boxes in flight.)
-    auto w_update = [&](float s_acc, float s_e, bool good) -> bool {
+    // With fill_next, each half also fills its own column blocks of the next matrix's X (the products
+    // that read them are done) in shares between its groups, so the loads overlap the TMA's drain.
+    auto w_update = [&](float s_acc, float s_e, bool good, bool fill_next) -> bool {
       uint8_t* stage = smem + kROff + warp * 8192;
       const uint32_t sbuf = smem_u32(stage);
       const int row0 = quarter * 32;
       const bool tma_w = job.tma_w && (p.w_alpha == 0.f || p.w_alpha == 1.f);
+      const SmallJob* nj = good && fill_next ? &p.jobs[j + gridDim.x] : nullptr;
+      const int fb_lo = half ? split / 64 : 0, fb_hi = half ? nb_next : min(split / 64, nb_next);
+      const int groups = max(0, (min(c_hi, n) - c_lo + 63) / 64), nparts = max(1, groups);
+      int filled = 0;
       if (good && row0 < m) {
         for (int c = c_lo; c < c_hi && c < n; c += 64) {
           float v[64];
@@ -386,6 +476,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1) ns_small_kernel(const __grid
               }
               bulk_commit();
             }
+            if (nj) fill_x(Xs, *nj, fb_lo, fb_hi, quarter * 32 + lane, 128, filled++, nparts);
           } else if (row < m) {
 #pragma unroll
             for (int k = 0; k < 64; ++k) {
@@ -398,6 +489,8 @@ __global__ void __launch_bounds__(kSmallThreads, 1) ns_small_kernel(const __grid
           }
         }
       }
+      if (nj)
+        for (; filled < nparts; ++filled) fill_x(Xs, *nj, fb_lo, fb_hi, quarter * 32 + lane, 128, filled, nparts);
       if (lane == 0) bulk_wait_read0();  // the staging area is R and Z: free it before the next matrix
       return phase_end(good);
     };
@@ -429,10 +522,8 @@ __global__ void __launch_bounds__(kSmallThreads, 1) ns_small_kernel(const __grid
       if (!alive) break;
       if (tid == 0) issue_times_x(sq);  // O = Q X
       const bool good = wait_half();
-      // The second barrier means every product of this matrix is done with X: fetch the next one now,
-      // under the weight update.
-      if (half == 1 && lane == 0 && quarter == 0 && good && has_next) issue_x(j + gridDim.x);
-      if (!w_update(1.f, 0.f, good)) break;
+      if (!w_update(1.f, 0.f, good, has_next)) break;
+      x_ready = has_next;
     } else {
       // ---- direct iteration
       for (int k = 0; alive && k < p.steps; ++k) {
@@ -442,7 +533,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1) ns_small_kernel(const __grid
         if (tid == 0) issue_times_x(smem_u32(Zs));                                         // B X
         if (k + 1 < p.steps) {
           if (!x_update(1.f, a)) { alive = false; break; }  // X = B X + a X
-        } else if (!w_update(1.f, a, wait_half(true))) {  // Z, in the staging area, is read by both halves
+        } else if (!w_update(1.f, a, wait_half(true), false)) {  // Z, in the staging area, is read by both halves
           alive = false;
           break;
         }
@@ -459,8 +550,6 @@ __global__ void __launch_bounds__(kSmallThreads, 1) ns_small_kernel(const __grid
     if (tid == 0) {
       mma_commit(&bar_mma[1]);
       wait_bounded(&bar_mma[1], mma_phase, abort_flag, p.status, kDrainLimitNs, false);
-      const int issued = *x_issued;
-      if (issued > 0) wait_bounded(bar_x, static_cast<uint32_t>(issued - 1) & 1u, abort_flag, p.status, kDrainLimitNs, false);
     }
   }
   tc_fence_before();
@@ -471,17 +560,18 @@ __global__ void __launch_bounds__(kSmallThreads, 1) ns_small_kernel(const __grid
 
 }  // namespace
 
-bool encode_small_job(SmallJob& job, const __half* X, int64_t ldx, float* W, int64_t ldw, int m, int n, bool trans,
-                      bool direct, const char** err) {
+bool encode_small_job(SmallJob& job, const float* M, int64_t ldm, const float* inv, float* W, int64_t ldw, int m,
+                      int n, bool trans, bool direct, const char** err) {
   job.direct = direct ? 1 : 0;
   job.m = m;
   job.n = n;
   job.trans = trans ? 1 : 0;
+  job.M = M;
+  job.ldm = ldm;
+  job.inv = inv;
+  job.vec_m = (reinterpret_cast<uintptr_t>(M) & 15) == 0 && (ldm & 3) == 0;
   job.W = W;
   job.ldw = ldw;
-  if (!encode_tensor_2d(&job.tmX, X, static_cast<uint64_t>(n), static_cast<uint64_t>(m), static_cast<uint64_t>(ldx) * 2,
-                        64, 128, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, CU_TENSOR_MAP_SWIZZLE_128B, err))
-    return false;
   job.tma_w = 0;
   if ((reinterpret_cast<uintptr_t>(W) & 15) == 0 && (ldw & 3) == 0) {
     const char* e2 = nullptr;
@@ -490,6 +580,7 @@ bool encode_small_job(SmallJob& job, const __half* X, int64_t ldx, float* W, int
                          CU_TENSOR_MAP_DATA_TYPE_FLOAT32, CU_TENSOR_MAP_SWIZZLE_128B, &e2))
       job.tma_w = 1;
   }
+  (void)err;
   return true;
 }
 

@@ -228,6 +228,11 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(r[k]);
 }
 
+// Prefetch [src, src + bytes) into L2 (src and bytes multiples of 16; no completion to wait for).
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // Start a load of 32 consecutive fp32 columns of this thread's TMEM lane into r[0, 32); the values may be
 // used only after tmem_ld_wait.
 __device__ __forceinline__ void tmem_ld32_issue(uint32_t taddr, uint32_t* r) {
