@@ -94,29 +94,35 @@ def total_flops(shapes, backend, restarts=(2,), dense=False):
 
 
 # The GEMM's DRAM traffic depends on the kernel and on the planner's tile order.
-GEMM_SOURCES = [os.path.join(ROOT, "newton_schulz_momentum_gb300", "csrc", f)
-                for f in ("gemm_tc.cu", "tc_ptx.h", "internal.h", "api.cu")]
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gemm_tc_dram_traffic.json")
+# Per workload: the committed ncu DRAM capture of its dominant kernel, and the sources that kernel's
+# traffic depends on (the capture is used only while their digest matches).
+TRAFFIC = {
+    "llama3-8b-muon-set": ("gemm_tc_dram_traffic.json", ("gemm_tc.cu", "tc_ptx.h", "internal.h", "api.cu")),
+    "small-set-2560": ("ns_small_dram_traffic.json", ("ns_small.cu", "tc_ptx.h", "internal.h", "api.cu")),
+}
 
 
-def gemm_source_digest():
+def source_digest(files):
     import hashlib
     h = hashlib.sha256()
-    for path in GEMM_SOURCES:
-        with open(path, "rb") as fh:
+    for f in files:
+        with open(os.path.join(ROOT, "newton_schulz_momentum_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()
 
 
 def measured_traffic(workload, backend):
-    """DRAM bytes per GEMM launch from the committed ncu capture, or None when the capture was taken on
-    another workload or an earlier version of the kernel source."""
+    """DRAM bytes per launch of the workload's dominant kernel from the committed ncu capture, or None
+    when there is none for this workload or it was taken on an earlier version of the kernel source."""
+    if workload not in TRAFFIC:
+        return None
+    fname, files = TRAFFIC[workload]
     try:
-        with open(TRAFFIC_FILE) as fh:
+        with open(os.path.join(ROOT, "profiles", fname)) as fh:
             rec = json.load(fh)
     except Exception:
         return None
-    if rec.get("kernel_source_sha256") != gemm_source_digest():
+    if rec.get("kernel_source_sha256") != source_digest(files):
         return None
     return rec.get("per_launch_bytes", {}).get(f"{workload}/{backend}")
 
@@ -465,7 +471,9 @@ def run_native(args):
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": tc_sust, "unit": "TFLOP/s",
                          "frac": (achieved / tc_sust) if achieved else None,
                          "traffic": measured_traffic(cfg["workload"], args.backend),
-                         "kernel": "gemm_tc_kernel (tcgen05 fp16, fp32 accumulate)",
+                         "kernel": ("ns_small_kernel (whole fused iteration per matrix: tcgen05 fp16, fp32 "
+                                    "accumulate; normalise/cast and weight update inside)") if fused_small
+                         else "gemm_tc_kernel (tcgen05 fp16, fp32 accumulate)",
                          "peak_source": f"{src} bf16 sustained (fp16 dense rate equals bf16)"},
             "cpu_baseline": cpu,
             "e2e": e2e,
