@@ -43,9 +43,10 @@ def parse():
     ap.add_argument("--backend", default="gram", choices=["gram", "direct", "auto"])
     ap.add_argument("--restarts", default="2", help="comma-separated restart indices for the Gram form ('' for none)")
     ap.add_argument("--layers", type=int, default=32)
-    ap.add_argument("--workload", default="llama", choices=["llama", "small", "adamw"],
+    ap.add_argument("--workload", default="llama", choices=["llama", "small", "adamw", "ns-configs"],
                     help="llama: Llama-3-8B Muon-target set (the headline); small: 2048 x 128x512 + 512 x 512x128; "
-                         "adamw: AdamW over the Llama-3-8B non-Muon parameters")
+                         "adamw: AdamW over the Llama-3-8B non-Muon parameters; ns-configs: the single "
+                         "256x1024 matrix and the closed-form 4096^2 and 2048x8192 dmuon_ns cases, both forms")
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--e2e-groups", type=int, default=0,
                     help="pipeline groups of the host-gradient call (0: the library's choice, 1: no overlap)")
@@ -617,6 +618,71 @@ def run_torch_mm_context(args):
                       "and flop count as the native arm; context only"}), flush=True)
 
 
+def run_ns_configs(args):
+    """The configurations beside the headline, timed one call at a time (CUDA events around each call on
+    the current stream, median over --steps after --warmup): the single 256 x 1024 matrix (one Muon
+    step, fp32 N(0, 1) gradient, YOU; latency-bound, reported in microseconds) and dmuon_ns on the
+    closed-form 4096 x 4096 matrix (singular values log-uniform in [1e-6, 1]) and 2048 x 8192 matrix (205
+    singular values 1, the rest 1e-4) with POLAR_EXPRESS, each in the Gram form (restart [2]) and the
+    direct form. dmuon_ns works in place, so each call starts from a fresh copy of the input, made before
+    its start event. Prints one JSON line."""
+    import statistics
+
+    import numpy as np
+    import torch
+
+    import newton_schulz_momentum_gb300 as dm
+    import workloads
+
+    dev = torch.device("cuda", 0)
+    _, tc_burst, _, src = peaks()
+
+    def timeit(fn, prep=None):
+        marks = []
+        for i in range(args.warmup + args.steps):
+            if prep is not None:
+                prep()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            if i >= args.warmup:
+                marks.append((a, b))
+        torch.cuda.synchronize(dev)
+        ms = [a.elapsed_time(b) for a, b in marks]
+        return statistics.median(ms), min(ms)
+
+    out = []
+    g = torch.from_numpy(workloads.gaussian((256, 1024), 1.0, 1)).to(dev)
+    for backend in ("gram", "direct"):
+        W, M = [torch.zeros((256, 1024), device=dev)], [torch.zeros((256, 1024), device=dev)]
+        step = dm.MuonStep(W, [g], M, coeffs=dm.YOU, restarts=(2,), backend=backend)
+        med, best = timeit(lambda: step(lr=LR, beta=BETA))
+        dm.check_status()
+        flops = dm.gram_flops(256, 1024) if backend == "gram" else dm.direct_flops(256, 1024)
+        out.append({"config": "single 256x1024, Muon step, fp32 grad, YOU", "backend": backend,
+                    "us_median": med * 1e3, "us_min": best * 1e3, "tflops": flops / (med * 1e-3) / 1e12,
+                    "bound": "latency"})
+    cases = (("4096x4096 closed form, sigma log-uniform in [1e-6, 1], POLAR_EXPRESS", 4096, 4096,
+              workloads.log_uniform_spectrum(4096, 1e-6, 1.0, 2), 2),
+             ("2048x8192 closed form, 205 sigma = 1, the rest 1e-4, POLAR_EXPRESS", 2048, 8192,
+              workloads.top_fraction_spectrum(2048, 0.1, 1.0, 1e-4), 3))
+    for name, m, n, sigma, seed in cases:
+        x0 = torch.from_numpy(workloads.closed_form_matrix(m, n, sigma, seed)[0].astype(np.float32)).to(dev)
+        x = torch.empty_like(x0)
+        for backend in ("gram", "direct"):
+            med, best = timeit(lambda: dm.ns(x, dm.POLAR_EXPRESS, (2,), backend), prep=lambda: x.copy_(x0))
+            dm.check_status()
+            flops = dm.gram_flops(m, n) if backend == "gram" else dm.direct_flops(m, n)
+            tf = flops / (med * 1e-3) / 1e12
+            out.append({"config": name, "backend": backend, "ms_median": med, "ms_min": best, "tflops": tf,
+                        "bound": "tensor", "frac_of_burst_peak": tf / tc_burst})
+    print(json.dumps({"impl": "native", "workload": "ns-configs", "steps": args.steps, "warmup": args.warmup,
+                      "dtype": "f16", "data": "synthetic", "peak_tflops_burst": tc_burst,
+                      "peak_source": f"{src} bf16 burst (fp16 dense rate equals bf16)", "results": out}),
+          flush=True)
+
+
 def main():
     args = parse()
     if args.impl == "reference":
@@ -625,6 +691,8 @@ def main():
         run_torch_mm_context(args)
     elif args.workload == "adamw":
         run_adamw(args)
+    elif args.workload == "ns-configs":
+        run_ns_configs(args)
     else:
         run_native(args)
 
