@@ -220,7 +220,9 @@ class MuonStep:
 
     With host_grads (CPU tensors shaped like grads, ideally pinned) each call is one
     dmuon_muon_step_host: the gradients are copied from host_grads into grads inside the call, in
-    `groups` pipelined groups (0: the library chooses) whose copies overlap the computation.
+    `groups` pipelined groups (0: the library chooses) whose copies overlap the computation. Many small
+    matrices (64 or more averaging under 4 MiB) are instead gathered by one kernel that reads host memory
+    directly, followed by the step as one group.
     """
 
     def __init__(self, params, grads, momenta, coeffs=POLAR_EXPRESS, restarts=DEFAULT_RESTARTS, backend="gram",
