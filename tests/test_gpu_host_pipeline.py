@@ -64,8 +64,10 @@ def _reference(dm, shapes, steps_grads, dtype, backend="gram"):
 
 
 def _pipelined(dm, shapes, steps_grads, dtype, groups, pinned=True, backend="gram"):
+    """pinned: True, False, or "mixed" (every other host buffer page-locked)."""
     W, M, G, norms = _state(shapes, dtype)
-    H = [torch.empty(s, dtype=dtype, pin_memory=pinned) for s in shapes]
+    H = [torch.empty(s, dtype=dtype, pin_memory=(i % 2 == 0) if pinned == "mixed" else pinned)
+         for i, s in enumerate(shapes)]
     out = []
     groups_seq = groups if isinstance(groups, (list, tuple)) else [groups] * len(steps_grads)
     for grads, g in zip(steps_grads, groups_seq):
@@ -142,7 +144,7 @@ MANY_SMALL = [(96, 200), (200, 96), (64, 64), (128, 512), (7, 1), (33, 130)] * 1
 MANY_MEDIUM = [(300, 264), (264, 520), (256, 256)] * 24                           # grouped GEMM plan
 
 
-@pytest.mark.parametrize("pinned", [True, False])
+@pytest.mark.parametrize("pinned", [True, False, "mixed"])
 @pytest.mark.parametrize("shapes", [MANY_SMALL, MANY_MEDIUM], ids=["fused", "grouped"])
 def test_many_small_matrices_gather(dm, shapes, pinned):
     steps = [_grads(shapes, 1300, torch.float32), _grads(shapes, 1400, torch.float32)]
