@@ -334,6 +334,7 @@ __device__ __forceinline__ void gemm_tc_body(const GemmLaunch& p) {
   const int unit = kPair ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
   const int nunits = kPair ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
 
+  griddep_launch_dependents();  // the next phase's CTAs may start their set-up as this grid's SMs free up
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&full[s], 1);
@@ -356,6 +357,7 @@ __device__ __forceinline__ void gemm_tc_body(const GemmLaunch& p) {
   if constexpr (kPair) cluster_sync_all();  // the peer's barriers are initialised before anyone signals them
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  griddep_wait();  // the previous phase's outputs are complete and visible before any global access
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
@@ -682,6 +684,23 @@ int gemm_max_units(int tile, int sms) {
   return cached[dev];
 }
 
+// Launched with programmatic stream serialisation: consecutive phases overlap launch and set-up (the
+// kernel waits for the previous grid before touching global memory).
+template <typename Kernel>
+cudaError_t launch_programmatic(Kernel kernel, unsigned grid, unsigned smem, const GemmLaunch& p, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(192, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, p);
+}
+
 cudaError_t launch_gemm(const GemmLaunch& p, int tile, int units, cudaStream_t stream) {
   if (p.ntiles <= 0) return cudaSuccess;
   cudaError_t e;
@@ -690,21 +709,22 @@ cudaError_t launch_gemm(const GemmLaunch& p, int tile, int units, cudaStream_t s
       e = cudaFuncSetAttribute(gemm_tc_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                Cfg<256, 2>::kSmemBytes);
       if (e != cudaSuccess) return e;
-      gemm_tc_pair_kernel<<<2 * units, 192, Cfg<256, 2>::kSmemBytes, stream>>>(p);
+      e = launch_programmatic(gemm_tc_pair_kernel, 2 * units, Cfg<256, 2>::kSmemBytes, p, stream);
       break;
     case kTileSingle256:
       e = cudaFuncSetAttribute(gemm_tc_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                Cfg<256, 1>::kSmemBytes);
       if (e != cudaSuccess) return e;
-      gemm_tc_kernel<256><<<units, 192, Cfg<256, 1>::kSmemBytes, stream>>>(p);
+      e = launch_programmatic(gemm_tc_kernel<256>, units, Cfg<256, 1>::kSmemBytes, p, stream);
       break;
     default:
       e = cudaFuncSetAttribute(gemm_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                Cfg<128, 1>::kSmemBytes);
       if (e != cudaSuccess) return e;
-      gemm_tc_kernel<128><<<units, 192, Cfg<128, 1>::kSmemBytes, stream>>>(p);
+      e = launch_programmatic(gemm_tc_kernel<128>, units, Cfg<128, 1>::kSmemBytes, p, stream);
       break;
   }
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

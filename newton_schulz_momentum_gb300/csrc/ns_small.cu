@@ -203,6 +203,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1) ns_small_kernel(const __grid
   const int half = warp >> 2;    // which half of each product's output columns this warp finishes
   const int row = quarter * 32 + lane;
 
+  griddep_launch_dependents();
   if (tid == 0) {
     mbar_init(&bar_mma[0], 1);
     mbar_init(&bar_mma[1], 1);
@@ -215,6 +216,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1) ns_small_kernel(const __grid
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const uint32_t my_tmem = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+  griddep_wait();  // the norm pass's results are complete and visible before any global access
 
   uint32_t mma_phase = 0;
   bool bad = false;
@@ -588,7 +590,20 @@ cudaError_t launch_ns_small(const SmallLaunch& p, int sms, cudaStream_t stream) 
   if (p.njobs <= 0) return cudaSuccess;
   cudaError_t e = cudaFuncSetAttribute(ns_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmallSmem);
   if (e != cudaSuccess) return e;
-  ns_small_kernel<<<std::min(p.njobs, sms), kSmallThreads, kSmallSmem, stream>>>(p);
+  // Programmatic stream serialisation: launch and set-up overlap the norm pass's tail; the kernel waits
+  // for it before touching global memory.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(std::min(p.njobs, sms)), 1, 1);
+  cfg.blockDim = dim3(kSmallThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmallSmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, ns_small_kernel, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -259,6 +259,12 @@ __device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[N]) {
 
 // ---------------------------------------------------------------------------- bulk stores and staging
 
+// Programmatic dependent launch: let the next kernel of the stream be scheduled now (its CTAs start as SMs
+// free up and run their set-up), and, in that next kernel, wait until every preceding grid has completed
+// and its memory is visible. Both are no-ops for a kernel launched without the programmatic attribute.
+__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t smem_src, int c0, int c1) {
