@@ -476,15 +476,35 @@ int pick_tile(int max_m, int max_n) {
   return kTilePair256;
 }
 
-int launch_tile(const std::vector<JobSpec>& ph) {
+// Output tiles of a launch under a tile configuration (symmetric products: upper-triangle tiles only).
+int64_t count_tiles(const std::vector<JobSpec>& ph, int tile) {
+  const int th = tile_rows(tile), tw = tile_cols(tile);
+  int64_t n = 0;
+  for (const JobSpec& js : ph) {
+    const int tm_n = (js.M + th - 1) / th, tn_n = (js.N + tw - 1) / tw;
+    for (int tm = 0; tm < tm_n; ++tm)
+      for (int tn = 0; tn < tn_n; ++tn)
+        if (!((js.flags & kJobSymmetric) && tn * tw + tw - 1 < tm * th)) ++n;
+  }
+  return n;
+}
+
+// A launch whose 256 x 256 pair tiles cannot fill the CTA pairs (a phase of a single matrix, or of a
+// few, of moderate size) runs on 128 x 128 single-CTA tiles instead: about four times the work units,
+// and half of a pair tile's epilogue per warp, for phases that would otherwise leave most SMs idle.
+int launch_tile(const std::vector<JobSpec>& ph, int pair_units) {
   int max_m = 0, max_n = 0;
   for (const JobSpec& j : ph) max_m = std::max(max_m, j.M), max_n = std::max(max_n, j.N);
-  return pick_tile(max_m, max_n);
+  const int tile = pick_tile(max_m, max_n);
+  const char* env = getenv("DMUON_GEMM_TILE");
+  if (tile == kTilePair256 && !(env && strcmp(env, "pair") == 0) && count_tiles(ph, kTilePair256) < pair_units)
+    return kTileSingle128;
+  return tile;
 }
 
 // Host-side plan: matrix layout, workspace offsets, phases, tiles. No device calls.
 int build_plan_host(Plan& pl, const PlanKey& key, const std::vector<const void*>& G, const std::vector<float*>& Mom,
-                    const std::vector<float*>& W, const std::vector<void*>& xout) {
+                    const std::vector<float*>& W, const std::vector<void*>& xout, int pair_units) {
   pl = Plan();
   pl.key = key;
   const int nm = static_cast<int>(key.rows.size());
@@ -640,7 +660,7 @@ int build_plan_host(Plan& pl, const PlanKey& key, const std::vector<const void*>
     LaunchRec L;
     L.first_job = 0;  // filled below
     L.njobs = static_cast<int>(ph.size());
-    L.tile = launch_tile(ph);
+    L.tile = launch_tile(ph, pair_units);
     L.coef = pl.phase_coef[p];
     L.group = pl.phase_group[p];
     L.first_tile = static_cast<int>(pl.tiles.size());
@@ -882,7 +902,7 @@ int ensure_plan(DeviceState& ds, const PlanKey& key, const std::vector<const voi
   if (ds.plan.bound && ds.plan.key == key) return DMUON_OK;
   if (rebuilt) *rebuilt = true;
   ds.plan = Plan();
-  int st = build_plan_host(ds.plan, key, G, Mom, W, xout);
+  int st = build_plan_host(ds.plan, key, G, Mom, W, xout, gemm_max_units(kTilePair256, ds.sms));
   if (st != DMUON_OK) return st;
   st = bind_plan(ds, ds.plan, stream);
   if (st != DMUON_OK) ds.plan = Plan();
@@ -1534,7 +1554,8 @@ int dmuon_workspace_size(int count, const int64_t* rows, const int64_t* cols, in
     std::vector<const void*> G(count, nullptr);
     std::vector<float*> Mo(count, nullptr), W(count, nullptr);
     std::vector<void*> xo(count, nullptr);
-    st = build_plan_host(pl, key, G, Mo, W, xo);
+    // No device here: the tile choice (and so the tile table's size) assumes GB300's 76 CTA pairs.
+    st = build_plan_host(pl, key, G, Mo, W, xo, 76);
     if (st != DMUON_OK) return st;
     *bytes_out = pl.bytes;
     return DMUON_OK;
