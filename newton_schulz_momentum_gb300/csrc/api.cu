@@ -842,10 +842,11 @@ int run_plan(DeviceState& ds, const Plan& pl, const float* coeffs, float lr, flo
               "momentum/sum-of-squares launch");
     }
     if (group_read) DM_CUDA(cudaEventRecord(group_read[g], stream), "record a group's gradients as read");
-    DM_CUDA(timed(1, stream, [&] { return launch_finalize_norms(rg, stream); }), "norm launch");
+    DM_CUDA(timed(1, stream, [&] { return launch_finalize_norms(rg, stream, true); }), "norm launch");
     // The fused small-matrix kernel normalises and casts as it reads M.
     if (!pl.small_fused)
-      DM_CUDA(timed(2, stream, [&] { return launch_normalize_cast(rg, ncast, stream); }), "normalise/cast launch");
+      DM_CUDA(timed(2, stream, [&] { return launch_normalize_cast(rg, ncast, stream, true); }),
+              "normalise/cast launch");
     if (pl.small_fused) {
       SmallLaunch sl;
       std::memset(&sl, 0, sizeof(sl));

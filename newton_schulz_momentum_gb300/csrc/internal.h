@@ -253,8 +253,10 @@ cudaError_t launch_h2d_gather(const GatherItem* items, const int64_t* prefix, in
 // Diagnostic: one bounded wait on an mbarrier phase that nothing completes (records kDevTimeout).
 cudaError_t launch_selftest_wait(unsigned* status, unsigned long long limit_ns, cudaStream_t stream);
 cudaError_t launch_momentum_sumsq(const RowLaunch& p, int64_t nchunks, cudaStream_t stream);
-cudaError_t launch_finalize_norms(const RowLaunch& p, cudaStream_t stream);
-cudaError_t launch_normalize_cast(const RowLaunch& p, int64_t ntiles, cudaStream_t stream);
+// programmatic: launched with programmatic stream serialisation (the planned path; the kernels wait for
+// the preceding grid themselves). The bulk momentum kernel (RowLaunch.status set) always is.
+cudaError_t launch_finalize_norms(const RowLaunch& p, cudaStream_t stream, bool programmatic = false);
+cudaError_t launch_normalize_cast(const RowLaunch& p, int64_t ntiles, cudaStream_t stream, bool programmatic = false);
 
 // Record `message` as the calling thread's last error (returned by dmuon_last_error) and return status.
 int set_error(int status, const char* message);

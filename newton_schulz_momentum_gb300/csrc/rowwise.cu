@@ -143,6 +143,10 @@ constexpr int kBulkSmem = kRingSlots * kSlotBytes + 64;
 static_assert(kChunkElems % kSub == 0, "a chunk is a whole number of slots");
 
 __global__ void __launch_bounds__(kThreads, 2) momentum_sumsq_bulk_kernel(const RowLaunch p) {
+  // Launched with programmatic stream serialisation: the next pass may be scheduled now; this one waits
+  // for the preceding grid before touching global memory.
+  ptx::griddep_launch_dependents();
+  ptx::griddep_wait();
   extern __shared__ __align__(128) uint8_t ring[];
   __shared__ float red[kThreads / 32];
   uint64_t* full = reinterpret_cast<uint64_t*>(ring + kRingSlots * kSlotBytes);
@@ -249,7 +253,7 @@ __global__ void __launch_bounds__(kThreads, 2) momentum_sumsq_bulk_kernel(const 
   if (threadIdx.x == 0) p.partials[mt.part_begin + local] = total;
 }
 
-__global__ void __launch_bounds__(kThreads) finalize_norms_kernel(const RowLaunch p) {
+__device__ __forceinline__ void finalize_norms_body(const RowLaunch& p) {
   __shared__ double red[kThreads / 32];
   const RowMat mt = p.mats[blockIdx.x];
   double s = 0.0;
@@ -263,6 +267,15 @@ __global__ void __launch_bounds__(kThreads) finalize_norms_kernel(const RowLaunc
   }
 }
 
+__global__ void __launch_bounds__(kThreads) finalize_norms_kernel(const RowLaunch p) { finalize_norms_body(p); }
+
+// The same, launched with programmatic stream serialisation (the planned path).
+__global__ void __launch_bounds__(kThreads) finalize_norms_pdl_kernel(const RowLaunch p) {
+  ptx::griddep_launch_dependents();
+  ptx::griddep_wait();
+  finalize_norms_body(p);
+}
+
 __device__ __forceinline__ void store_half4(__half* dst, float a, float b, float c, float d) {
   __half2 lo = __floats2half2_rn(a, b), hi = __floats2half2_rn(c, d);
   uint2 u;
@@ -271,7 +284,7 @@ __device__ __forceinline__ void store_half4(__half* dst, float a, float b, float
   *reinterpret_cast<uint2*>(dst) = u;
 }
 
-__global__ void __launch_bounds__(kThreads) normalize_cast_kernel(const RowLaunch p) {
+__device__ __forceinline__ void normalize_cast_body(const RowLaunch& p) {
   __shared__ float tile[kCastTile][kCastTile + 1];
   const int64_t t = p.tile_base + blockIdx.x;
   const int mi = find_matrix(p.tile_prefix, p.nmats, t);
@@ -369,6 +382,15 @@ __global__ void __launch_bounds__(kThreads) normalize_cast_kernel(const RowLaunc
         if (xc + k < mt.rows) dst[k] = __float2half_rn(tile[rr + k][cc] * inv);
     }
   }
+}
+
+__global__ void __launch_bounds__(kThreads) normalize_cast_kernel(const RowLaunch p) { normalize_cast_body(p); }
+
+// The same, launched with programmatic stream serialisation (the planned path).
+__global__ void __launch_bounds__(kThreads) normalize_cast_pdl_kernel(const RowLaunch p) {
+  ptx::griddep_launch_dependents();
+  ptx::griddep_wait();
+  normalize_cast_body(p);
 }
 
 // Sum of squares of one shard (columns [bounds[t], bounds[t+1]) of the oriented matrix) over one slab of
@@ -470,27 +492,54 @@ cudaError_t launch_selftest_wait(unsigned* status, unsigned long long limit_ns, 
   return cudaGetLastError();
 }
 
+// A launch with programmatic stream serialisation (the kernel waits for the preceding grid itself).
+template <typename Kernel>
+cudaError_t launch_programmatic(Kernel kernel, unsigned grid, unsigned smem, const RowLaunch& p, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, p);
+}
+
 cudaError_t launch_momentum_sumsq(const RowLaunch& p, int64_t nchunks, cudaStream_t stream) {
   if (nchunks <= 0) return cudaSuccess;
   if (p.status) {
     cudaError_t e = cudaFuncSetAttribute(momentum_sumsq_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kBulkSmem);
     if (e != cudaSuccess) return e;
-    momentum_sumsq_bulk_kernel<<<static_cast<unsigned>(nchunks), kThreads, kBulkSmem, stream>>>(p);
+    e = launch_programmatic(momentum_sumsq_bulk_kernel, static_cast<unsigned>(nchunks), kBulkSmem, p, stream);
+    if (e != cudaSuccess) return e;
   } else {
     momentum_sumsq_kernel<<<static_cast<unsigned>(nchunks), kThreads, 0, stream>>>(p);
   }
   return cudaGetLastError();
 }
 
-cudaError_t launch_finalize_norms(const RowLaunch& p, cudaStream_t stream) {
-  finalize_norms_kernel<<<p.nmats, kThreads, 0, stream>>>(p);
+cudaError_t launch_finalize_norms(const RowLaunch& p, cudaStream_t stream, bool programmatic) {
+  if (programmatic) {
+    const cudaError_t e = launch_programmatic(finalize_norms_pdl_kernel, static_cast<unsigned>(p.nmats), 0, p, stream);
+    if (e != cudaSuccess) return e;
+  } else {
+    finalize_norms_kernel<<<p.nmats, kThreads, 0, stream>>>(p);
+  }
   return cudaGetLastError();
 }
 
-cudaError_t launch_normalize_cast(const RowLaunch& p, int64_t ntiles, cudaStream_t stream) {
+cudaError_t launch_normalize_cast(const RowLaunch& p, int64_t ntiles, cudaStream_t stream, bool programmatic) {
   if (ntiles <= 0) return cudaSuccess;
-  normalize_cast_kernel<<<static_cast<unsigned>(ntiles), kThreads, 0, stream>>>(p);
+  if (programmatic) {
+    const cudaError_t e = launch_programmatic(normalize_cast_pdl_kernel, static_cast<unsigned>(ntiles), 0, p, stream);
+    if (e != cudaSuccess) return e;
+  } else {
+    normalize_cast_kernel<<<static_cast<unsigned>(ntiles), kThreads, 0, stream>>>(p);
+  }
   return cudaGetLastError();
 }
 
