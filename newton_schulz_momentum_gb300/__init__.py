@@ -7,6 +7,9 @@ call raises ``LibraryNotBuilt``.
     import newton_schulz_momentum_gb300 as dm
     dm.ns(x, dm.POLAR_EXPRESS, restarts=(2,), backend="gram")          # in place, fp32 CUDA tensor
     dm.muon_step(params, grads, momenta, lr=0.02, beta=0.95, coeffs=dm.POLAR_EXPRESS)
+
+The pages' own names -- newton_schulz, NewtonSchulz and the Muon optimizer -- live in
+newton_schulz_momentum_gb300.optim (imports torch) and are reachable here as attributes.
 """
 
 from __future__ import annotations
@@ -447,3 +450,12 @@ def direct_flops(m, n, steps=5, dense=False):
     m, n = min(m, n), max(m, n)
     h = 2 if dense else 1
     return steps * ((h + 2) * m * m * n + h * m ** 3)
+
+
+def __getattr__(name):
+    """newton_schulz, NewtonSchulz, Muon and default_muon_filter load from .optim on first use (it imports
+    torch; this module does not)."""
+    if name in ("newton_schulz", "NewtonSchulz", "Muon", "default_muon_filter"):
+        from . import optim
+        return getattr(optim, name)
+    raise AttributeError(f"module {__name__!r} has no attribute {name!r}")
