@@ -136,7 +136,8 @@ DMUON_API int dmuon_muon_step(int count, float* const* params, const void* const
  * ranks, not from the host; this is the single-GPU form of "gradients in, update out".) Equivalent to
  * copying every grads_host[i] into grads[i] and then calling dmuon_muon_step, with identical results,
  * but the copies overlap the computation: the matrices are taken in `groups` consecutive groups by
- * gradient bytes (the first half the size of the others, since its copy is the one left exposed);
+ * gradient bytes, in the weights 1 : 3 : 7 : 7 : ... (the first group's copy is the one left exposed, and
+ * each later copy must fit under the previous group's computation);
  * group g's copies run on the library's copy stream while earlier groups compute on
  * cuda_stream, and group g's momentum pass waits only for its own copies. Each group runs its row-wise
  * passes and Newton-Schulz phases as grouped launches of its own. With many small matrices (64 or more

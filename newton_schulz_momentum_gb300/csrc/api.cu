@@ -602,20 +602,28 @@ int build_plan_host(Plan& pl, const PlanKey& key, const std::vector<const void*>
                                          : static_cast<int>(pl.chunk_prefix[i + 1] - pl.chunk_prefix[i]);
     part += r.part_count;
   }
-  // Matrix groups: consecutive runs of gradient bytes, the first holding half the share of each later
-  // one (its copy is the only one not hidden behind computation): boundary g sits at the cumulative share
-  // (2g - 1) / (2 ng - 1). One group for every other plan.
+  // Matrix groups: consecutive runs of gradient bytes in the weights 1 : 3 : 7 : 7 : ... Only the first
+  // group's copy is exposed, so it is small; each later copy has to fit under the previous group's
+  // computation, which takes several times as long as copying the same bytes, so the shares can grow
+  // threefold and then about twofold. Boundary g sits at the cumulative weight of groups 0 .. g-1. One
+  // group for every other plan.
   {
     const int ng = (key.kind == kPlanMuon && !pl.small_fused) ? std::max(1, std::min(key.groups, nm)) : 1;
+    auto weight = [](int g) -> int64_t { return g == 0 ? 1 : g == 1 ? 3 : 7; };
+    int64_t wsum = 0;
+    for (int g = 0; g < ng; ++g) wsum += weight(g);
     pl.group_begin.assign(1, 0);
     int64_t total = 0;
     for (int i = 0; i < nm; ++i) total += pl.mats[i].rows * pl.mats[i].cols;
-    int64_t run = 0;
+    int64_t run = 0, wcum = weight(0);  // cumulative weight up to the boundary being placed
     for (int i = 0; i < nm && static_cast<int>(pl.group_begin.size()) < ng; ++i) {
       run += pl.mats[i].rows * pl.mats[i].cols;
       const int g = static_cast<int>(pl.group_begin.size());  // boundary being placed
       // Close group g - 1 after matrix i once it holds its share, leaving a matrix for each later group.
-      if (run * (2 * ng - 1) >= total * (2 * g - 1) && nm - (i + 1) >= ng - g) pl.group_begin.push_back(i + 1);
+      if (run * wsum >= total * wcum && nm - (i + 1) >= ng - g) {
+        pl.group_begin.push_back(i + 1);
+        wcum += weight(g);
+      }
     }
     pl.group_begin.push_back(nm);
   }
