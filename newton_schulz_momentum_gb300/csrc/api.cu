@@ -999,7 +999,7 @@ int ensure_gather(DeviceState& ds, int count, const void* const* src, void* cons
   for (int i = 0; i < count; ++i) {
     const void* s = resolve(i);
     if (!s) {
-      ds.gather_key = key;  // remember the verdict for this pointer set
+      ds.gather_key = key;  // remember the outcome for this pointer set
       return DMUON_OK;
     }
     items[i] = GatherItem{s, dst[i], bytes[i]};
