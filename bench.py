@@ -624,7 +624,8 @@ def run_ns_configs(args):
     step, fp32 N(0, 1) gradient, YOU; latency-bound, reported in microseconds) and dmuon_ns on the
     closed-form 4096 x 4096 matrix (singular values log-uniform in [1e-6, 1]) and 2048 x 8192 matrix (205
     singular values 1, the rest 1e-4) with POLAR_EXPRESS, each in the Gram form (restart [2]) and the
-    direct form. dmuon_ns works in place, so each call starts from a fresh copy of the input, made before
+    direct form; the 2048 x 8192 case also through dmuon_ns_tp split into 2 and 8 column shards. dmuon_ns
+    works in place, so each call starts from a fresh copy of the input, made before
     its start event. Prints one JSON line."""
     import statistics
 
@@ -677,6 +678,16 @@ def run_ns_configs(args):
             tf = flops / (med * 1e-3) / 1e12
             out.append({"config": name, "backend": backend, "ms_median": med, "ms_min": best, "tflops": tf,
                         "bound": "tensor", "frac_of_burst_peak": tf / tc_burst})
+        if m == 2048:
+            # The column-split (tensor-parallel exact) Gram form emulated on this GPU: every Gram formation is
+            # `shards` per-shard products written in fp32, then the fixed-order reduction.
+            for shards in (2, 8):
+                med, best = timeit(lambda: dm.ns_tp(x, shards, dm.POLAR_EXPRESS, (2,)), prep=lambda: x.copy_(x0))
+                dm.check_status()
+                tf = dm.gram_flops(m, n) / (med * 1e-3) / 1e12
+                out.append({"config": name, "backend": f"gram, {shards} column shards (dmuon_ns_tp)",
+                            "ms_median": med, "ms_min": best, "tflops": tf, "bound": "tensor",
+                            "frac_of_burst_peak": tf / tc_burst})
     print(json.dumps({"impl": "native", "workload": "ns-configs", "steps": args.steps, "warmup": args.warmup,
                       "dtype": "f16", "data": "synthetic", "peak_tflops_burst": tc_burst,
                       "peak_source": f"{src} bf16 burst (fp16 dense rate equals bf16)", "results": out}),
