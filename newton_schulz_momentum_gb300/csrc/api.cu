@@ -529,7 +529,8 @@ int build_plan_host(Plan& pl, const PlanKey& key, const std::vector<const void*>
     mi.W = W[i];
     mi.xout = xout[i];
     const int64_t numel = mi.rows * mi.cols;
-    pl.chunk_prefix[i + 1] = pl.chunk_prefix[i] + (numel + kChunkElems - 1) / kChunkElems;
+    const int64_t chunk = momentum_chunk(numel);
+    pl.chunk_prefix[i + 1] = pl.chunk_prefix[i] + (numel + chunk - 1) / chunk;
     pl.tile_prefix[i + 1] =
         pl.tile_prefix[i] + ((mi.rows + kCastTile - 1) / kCastTile) * ((mi.cols + kCastTile - 1) / kCastTile);
   }
@@ -597,6 +598,7 @@ int build_plan_host(Plan& pl, const PlanKey& key, const std::vector<const void*>
     r.gdtype = key.gdtype;
     r.trans = mi.trans ? 1 : 0;
     r.vec_ok = 1;  // pointers are validated 16-byte aligned
+    r.chunk = momentum_chunk(mi.rows * mi.cols);
     r.part_begin = part;
     r.part_count = key.kind == kPlanNsTp ? key.shards * pl.tp_slabs
                                          : static_cast<int>(pl.chunk_prefix[i + 1] - pl.chunk_prefix[i]);

@@ -161,7 +161,21 @@ struct RowMat {
   int vec_ok;     // pointers and rows allow 16-byte vector access
   int part_begin, part_count;  // this matrix's partial sums
   int pad_;
+  // Elements per momentum chunk of this matrix in the bulk-copy pass (a multiple of 4096). It depends on
+  // the matrix alone, so a matrix's norm is summed the same way whatever else is in the call. The
+  // vector-load pass of the allocation-free entry uses kChunkElems.
+  int64_t chunk;
 };
+
+// The bulk-copy pass's chunk for a matrix of `numel` elements: one chunk up to kChunkElems, 64 chunks up
+// to 64 kChunkElems (a lone matrix of moderate size is spread over many CTAs instead of a few making
+// long trips through their copy ring), kChunkElems beyond.
+inline int64_t momentum_chunk(int64_t numel) {
+  if (numel <= kChunkElems) return kChunkElems;
+  int64_t c = kChunkElems;
+  while (c > 4096 && c * 64 > numel) c /= 2;
+  return c;
+}
 
 struct RowLaunch {
   const RowMat* mats;

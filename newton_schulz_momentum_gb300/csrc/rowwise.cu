@@ -156,8 +156,8 @@ __global__ void __launch_bounds__(kThreads, 2) momentum_sumsq_bulk_kernel(const 
   const RowMat mt = p.mats[mi];
   const int64_t local = chunk - p.chunk_prefix[mi];
   const int64_t numel = mt.rows * mt.cols;
-  const int64_t begin = local * kChunkElems;
-  const int64_t end = min(begin + static_cast<int64_t>(kChunkElems), numel);
+  const int64_t begin = local * mt.chunk;
+  const int64_t end = min(begin + mt.chunk, numel);
   const bool has_g = mt.G != nullptr;
   const int gsize = mt.gdtype == 1 ? 2 : 4;
   const float beta = p.beta;
