@@ -357,7 +357,19 @@ __device__ __forceinline__ void gemm_tc_body(const GemmLaunch& p) {
   if constexpr (kPair) cluster_sync_all();  // the peer's barriers are initialised before anyone signals them
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  griddep_wait();  // the previous phase's outputs are complete and visible before any global access
+  // The tile list and the tensor maps were written when the plan was bound, never by a kernel: fetch the
+  // first tile's maps while the previous grid finishes.
+  if (warp == 0 && lane == 0 && unit < p.ntiles) {
+    const TileRef tr0 = tile_at(p, unit, BN, C::kTileM);
+    prefetch_tensormap(&tr0.job->tmA);
+    prefetch_tensormap(&tr0.job->tmB);
+    if (tr0.job->flags & kJobFinal) {
+      if (tr0.job->flags & kJobTmaW) prefetch_tensormap(&tr0.job->tmW);
+    } else {
+      prefetch_tensormap(&tr0.job->tmD);
+    }
+  }
+  griddep_wait();  // the previous phase's outputs are complete and visible before any other global access
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer

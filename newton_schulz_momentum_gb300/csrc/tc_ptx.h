@@ -259,6 +259,11 @@ __device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[N]) {
 
 // ---------------------------------------------------------------------------- bulk stores and staging
 
+// Fetch a tensor map's descriptor ahead of its first TMA use.
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
+}
+
 // Programmatic dependent launch: let the next kernel of the stream be scheduled now (its CTAs start as SMs
 // free up and run their set-up), and, in that next kernel, wait until every preceding grid has completed
 // and its memory is visible. Both are no-ops for a kernel launched without the programmatic attribute.
