@@ -343,10 +343,22 @@ def run_e2e(args, G, norms, make_host_step, barrier, stream, world, flops_step):
     stop.record(stream)
     barrier()
     ms = max_over_ranks(start.elapsed_time(stop), norms.device)
+    # This machine's host link, measured on the same buffers right after (plain copies of every gradient, no
+    # computation): the end-to-end step cannot beat max(device step, this copy time), and the link rate
+    # differs a lot between hosts.
+    la, lb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        la.record(stream)
+        for g, h in zip(G, host_g):
+            g.copy_(h, non_blocking=True)
+        lb.record(stream)
+    lb.synchronize()
+    link_ms = la.elapsed_time(lb)
     del host_g
     return {"value": whole_job_tflops(flops_step, world, ms / args.e2e_steps), "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms / args.e2e_steps,
-            "warmup_passes": passes}
+            "warmup_passes": passes, "h2d_link_gbs_this_box": h2d / (link_ms * 1e-3) / 1e9,
+            "h2d_copy_ms_this_box": link_ms}
 
 
 def run_native(args):
