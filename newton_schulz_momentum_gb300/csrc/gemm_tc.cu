@@ -16,6 +16,12 @@
 //               one output row per thread), combine with the step's scalars and an optional fp16
 //               addend, store fp16 (mirrored for symmetric outputs) or update the fp32 weights.
 // The accumulator is double-buffered so a tile's epilogue overlaps the next tile's main loop.
+// Three tile configurations: 256 x 256 tiles on CTA pairs (a cluster of two; tcgen05.mma.cta_group::2,
+// each CTA holding half of A and half of B per stage), 128 x 256 and 128 x 128 on single CTAs; the
+// planner takes the pair tiles unless a launch could not fill the pairs or its products are at most 128
+// wide. Launches are programmatic: a grid lets the next phase be scheduled at entry, and sets up its
+// barriers and tensor memory (and prefetches its first tensor maps) before waiting for the previous
+// grid.
 //
 // Every mbarrier wait is bounded: after kWaitLimitNs the waiting thread raises a CTA-wide abort
 // flag and sets kDevTimeout in the device status word, all roles leave their loops, in-flight copies

@@ -4,7 +4,9 @@
 // section "重启机制", or the direct iteration of section "直接空间 NS（经典）").
 //
 // Shared memory holds every operand in the 128-byte-swizzled layout tcgen05 reads directly: X (up to
-// 8 column blocks of 128 rows x 64 fp16) and R, Z, Q (2 blocks each). A K-major A operand, a K-major B
+// 8 column blocks of 128 rows x 64 fp16) and R, Z, Q (2 blocks each). X is built there from the fp32
+// momentum and the norm pass's 1 / (||M|| + eps) (the normalise-and-cast step of the row-wise pass,
+// with the same rounding), so no fp16 copy of X goes through HBM. A K-major A operand, a K-major B
 // operand (rows = output columns) and an MN-major B operand (rows = the contraction index) are all views of
 // this one row-major layout, so each product is issued exactly as written: X X^T reads X as a K-major B;
 // the m x m products (R R, Z Q, Z R, S Z) read their right factor MN-major, with no assumption that it is
@@ -21,7 +23,9 @@
 // reads only its own column blocks of X. fp16 overflow is tracked with one packed FMA per pair of
 // values. Rows and columns beyond the matrix are kept at zero. The final Q X (or B X + a X) goes out as
 // W += w_beta * O by TMA reduce-add (TMA store when W is overwritten, direct stores when W rows are not
-// 16-byte aligned); in the Gram form the next matrix's X is fetched under it. Every wait is bounded.
+// 16-byte aligned); in the Gram form the next matrix's X is built under it (its M was prefetched into L2
+// at the start of the current matrix). The launch is programmatic: set-up overlaps the norm pass's tail,
+// and the kernel waits for it before touching global memory. Every wait is bounded.
 #include <algorithm>
 
 #include "internal.h"

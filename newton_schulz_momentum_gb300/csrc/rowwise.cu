@@ -5,7 +5,10 @@
 //                       inv = 1 / (||M||_F + eps) ("Newton-Schulz 变体", section "精度流水线");
 //   3. normalize_cast   X = fp16(M * inv), written in the m <= n orientation (tall matrices are
 //                       transposed through shared memory) -- the fp16 input of the iteration.
-// Reductions are deterministic: fixed chunking, fixed tree order, no atomics.
+// Reductions are deterministic: fixed chunking (per matrix, so a matrix's norm does not depend on the
+// rest of the call), fixed tree order, no atomics. The planned path launches all three programmatically
+// (each waits for the preceding grid before touching global memory); the allocation-free entry launches
+// the same bodies plainly.
 #include "internal.h"
 #include "tc_ptx.h"
 
