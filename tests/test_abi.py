@@ -5,6 +5,7 @@ and flop accounting agree with closed forms."""
 import ctypes
 import os
 import re
+import subprocess
 
 import pytest
 
@@ -22,7 +23,8 @@ def L():
 
 
 def header_functions():
-    src = open(os.path.join(ROOT, "include", "dmuon.h")).read()
+    with open(os.path.join(ROOT, "include", "dmuon.h")) as f:
+        src = f.read()
     return sorted(set(re.findall(r"DMUON_API\s+[\w\s\*]+?\b(dmuon_\w+)\s*\(", src)))
 
 
@@ -32,7 +34,8 @@ def test_exports_match_header(L):
     assert sorted(dm.EXPORTS) == declared
     for name in declared:
         assert hasattr(L, name), name
-    out = os.popen(f"nm -D --defined-only {dm.LIB_PATH}").read()
+    out = subprocess.run(["nm", "-D", "--defined-only", dm.LIB_PATH], check=True,
+                         capture_output=True, text=True).stdout
     exported = sorted(set(re.findall(r" T (dmuon_\w+)", out)))
     assert exported == declared
 

@@ -35,7 +35,8 @@ def test_stale_digest_hides_the_capture(tmp_path, monkeypatch):
     src = os.path.join(bench.ROOT, "profiles", fname)
     if not os.path.exists(src):
         pytest.skip("no committed capture")
-    rec = json.load(open(src))
+    with open(src) as f:
+        rec = json.load(f)
     rec["kernel_source_sha256"] = "0" * 64
     (tmp_path / "profiles").mkdir()
     (tmp_path / "profiles" / fname).write_text(json.dumps(rec))
