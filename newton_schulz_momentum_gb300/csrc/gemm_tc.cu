@@ -7,7 +7,7 @@
 // jobs (one job = one product on one matrix), so all matrices a rank owns advance one phase per
 // launch.
 //
-// CTA layout (192 threads, one persistent CTA per SM):
+// CTA layout (192 threads, or 320 for 128 x 128 tiles; one persistent CTA per SM):
 //   warp 0      TMA producer: one thread streams 128 x 64 A tiles and BN x 64 B tiles into a
 //               STAGES-deep ring of 128-byte-swizzled shared memory buffers.
 //   warp 1      allocates tensor memory; one thread issues tcgen05.mma (M=128, N=BN, K=16) into one
@@ -15,6 +15,8 @@
 //   warps 2-5   epilogue: tcgen05.ld the accumulator (warp w reads TMEM lanes 32*(w%4)..+31, i.e.
 //               one output row per thread), combine with the step's scalars and an optional fp16
 //               addend, store fp16 (mirrored for symmetric outputs) or update the fp32 weights.
+//               128 x 128 tiles run only in launches too small to fill the machine, where the
+//               epilogue is the critical path: warps 2-9, two per lane quarter, each half the columns.
 // The accumulator is double-buffered so a tile's epilogue overlaps the next tile's main loop.
 // Three tile configurations: 256 x 256 tiles on CTA pairs (a cluster of two; tcgen05.mma.cta_group::2,
 // each CTA holding half of A and half of B per stage), 128 x 256 and 128 x 128 on single CTAs; the
@@ -48,7 +50,11 @@ struct Cfg {
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kStages = (kStageBytes <= 32768) ? 6 : 4;
   static constexpr int kTmemCols = 2 * BN;  // two accumulators of BN fp32 columns
-  static constexpr int kEpiBytes = 4 * 4096;  // one 4 KB staging buffer per epilogue warp
+  // Epilogue warps: one per TMEM lane quarter, or two (each draining half of the tile's columns) for the
+  // 128 x 128 tiles of launches too small to fill the machine, whose epilogue is their critical path.
+  static constexpr int kEpiWarps = (BN == 128 && CG == 1) ? 8 : 4;
+  static constexpr int kThreads = 64 + 32 * kEpiWarps;
+  static constexpr int kEpiBytes = kEpiWarps * 4096;  // one 4 KB staging buffer per epilogue warp
   static constexpr int kBarrierBytes = 256;
   static constexpr int kSmemBytes = kStages * kStageBytes + kEpiBytes + kBarrierBytes + 1024;  // + alignment slack
   static_assert(kStageBytes % 1024 == 0, "stages must keep 1024-byte alignment for 128B swizzle");
@@ -127,9 +133,11 @@ __device__ __forceinline__ void reduce_out(const CUtensorMap* map, uint32_t src,
   else tma_reduce_add_2d(map, src, c0, c1);
 }
 
+// One warp's share of a tile: the 32 rows of TMEM lane quarter `quarter`, columns [c_lo, c_hi) of the tile.
 template <int BN>
 __device__ void epilogue_tile(const GemmLaunch& p, const GemmJob& job, int tile_row0, int tn, int quarter,
-                              int lane, uint32_t taddr, uint8_t* stage, bool& bad, uint64_t pol_out) {
+                              int c_lo, int c_hi, int lane, uint32_t taddr, uint8_t* stage, bool& bad,
+                              uint64_t pol_out) {
   const int row0 = tile_row0 + quarter * 32;  // first row handled by this warp
   if (row0 >= job.M) return;                  // all 32 rows past the edge: nothing to read or store
   const int i = row0 + lane;
@@ -154,21 +162,21 @@ __device__ void epilogue_tile(const GemmLaunch& p, const GemmJob& job, int tile_
 
   // Symmetric outputs: chunks left of the diagonal block are produced by the mirrored stores of other
   // tiles, so this warp starts at its diagonal block (row0 and tn*BN are multiples of 32).
-  int c = sym ? max(0, row0 - tn * BN) : 0;
+  int c = sym ? max(c_lo, row0 - tn * BN) : c_lo;
   uint4 ecur[4], enext[4];
 #pragma unroll
   for (int q = 0; q < 4; ++q) ecur[q] = make_uint4(0, 0, 0, 0), enext[q] = ecur[q];
-  if (erow && c < BN && tn * BN + c + 32 <= job.N) {
+  if (erow && c < c_hi && tn * BN + c + 32 <= job.N) {
     const uint4* e4 = reinterpret_cast<const uint4*>(erow + tn * BN + c);
 #pragma unroll
     for (int q = 0; q < 4; ++q) ecur[q] = e4[q];
   }
 
-  for (; c < BN; c += 32) {
+  for (; c < c_hi; c += 32) {
     const int j0 = tn * BN + c;
     if (j0 >= job.N) break;  // warp-uniform
     const bool full = j0 + 32 <= job.N;
-    const bool prefetch = erow != nullptr && c + 32 < BN && j0 + 64 <= job.N;
+    const bool prefetch = erow != nullptr && c + 32 < c_hi && j0 + 64 <= job.N;
     if (prefetch) {
       const uint4* e4 = reinterpret_cast<const uint4*>(erow + j0 + 32);
 #pragma unroll
@@ -348,7 +356,7 @@ __device__ __forceinline__ void gemm_tc_body(const GemmLaunch& p) {
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 4 * CG);  // every epilogue warp of the pair releases the accumulator
+      mbar_init(&tempty[a], C::kEpiWarps * CG);  // every epilogue warp of the pair releases the accumulator
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -521,8 +529,10 @@ __device__ __forceinline__ void gemm_tc_body(const GemmLaunch& p) {
       wait_bounded(drain, 0, abort_flag, p.status, kDrainLimitNs, false);
     }
   } else {
-    // ------------------------------------------------------------------ epilogue (warps 2..5)
+    // ------------------------------------------------------------------ epilogue (warps 2 .. 1 + kEpiWarps)
     const int quarter = warp & 3;  // TMEM lanes this warp may access
+    constexpr int kSpan = BN / (C::kEpiWarps / 4);    // columns per warp
+    const int c_lo = ((warp - 2) >> 2) * kSpan;
     const uint64_t pol_out = l2_policy_evict_first();
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -536,8 +546,8 @@ __device__ __forceinline__ void gemm_tc_body(const GemmLaunch& p) {
       tc_fence_after();
       const uint32_t taddr =
           tmem_base + static_cast<uint32_t>(acc * BN) + (static_cast<uint32_t>(quarter * 32) << 16);
-      epilogue_tile<BN>(p, *tr.job, tr.tm * C::kTileM + static_cast<int>(rank) * kBM, tr.tn, quarter, lane, taddr,
-                        epi_stage + (warp - 2) * 4096, bad, pol_out);
+      epilogue_tile<BN>(p, *tr.job, tr.tm * C::kTileM + static_cast<int>(rank) * kBM, tr.tn, quarter, c_lo,
+                        c_lo + kSpan, lane, taddr, epi_stage + (warp - 2) * 4096, bad, pol_out);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
@@ -571,12 +581,12 @@ __device__ __forceinline__ void gemm_tc_body(const GemmLaunch& p) {
 }
 
 template <int BN>
-__global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__ GemmLaunch p) {
+__global__ void __launch_bounds__(Cfg<BN, 1>::kThreads, 1) gemm_tc_kernel(const __grid_constant__ GemmLaunch p) {
   gemm_tc_body<BN, 1>(p);
 }
 
 // CTA pairs: a 256 x 256 output tile per pair, one tcgen05.mma.cta_group::2 stream issued by the leader.
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1) gemm_tc_pair_kernel(const __grid_constant__ GemmLaunch p) {
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<256, 2>::kThreads, 1) gemm_tc_pair_kernel(const __grid_constant__ GemmLaunch p) {
   gemm_tc_body<256, 2>(p);
 }
 
@@ -684,7 +694,7 @@ int gemm_max_units(int tile, int sms) {
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(sms & ~1), 1, 1);
-  cfg.blockDim = dim3(192, 1, 1);
+  cfg.blockDim = dim3(Cfg<256, 2>::kThreads, 1, 1);
   cfg.dynamicSmemBytes = Cfg<256, 2>::kSmemBytes;
   cudaLaunchAttribute attr;
   attr.id = cudaLaunchAttributeClusterDimension;
@@ -705,10 +715,11 @@ int gemm_max_units(int tile, int sms) {
 // Launched with programmatic stream serialisation: consecutive phases overlap launch and set-up (the
 // kernel waits for the previous grid before touching global memory).
 template <typename Kernel>
-cudaError_t launch_programmatic(Kernel kernel, unsigned grid, unsigned smem, const GemmLaunch& p, cudaStream_t stream) {
+cudaError_t launch_programmatic(Kernel kernel, unsigned grid, unsigned threads, unsigned smem, const GemmLaunch& p,
+                                cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid, 1, 1);
-  cfg.blockDim = dim3(192, 1, 1);
+  cfg.blockDim = dim3(threads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -727,19 +738,19 @@ cudaError_t launch_gemm(const GemmLaunch& p, int tile, int units, cudaStream_t s
       e = cudaFuncSetAttribute(gemm_tc_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                Cfg<256, 2>::kSmemBytes);
       if (e != cudaSuccess) return e;
-      e = launch_programmatic(gemm_tc_pair_kernel, 2 * units, Cfg<256, 2>::kSmemBytes, p, stream);
+      e = launch_programmatic(gemm_tc_pair_kernel, 2 * units, Cfg<256, 2>::kThreads, Cfg<256, 2>::kSmemBytes, p, stream);
       break;
     case kTileSingle256:
       e = cudaFuncSetAttribute(gemm_tc_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                Cfg<256, 1>::kSmemBytes);
       if (e != cudaSuccess) return e;
-      e = launch_programmatic(gemm_tc_kernel<256>, units, Cfg<256, 1>::kSmemBytes, p, stream);
+      e = launch_programmatic(gemm_tc_kernel<256>, units, Cfg<256, 1>::kThreads, Cfg<256, 1>::kSmemBytes, p, stream);
       break;
     default:
       e = cudaFuncSetAttribute(gemm_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                Cfg<128, 1>::kSmemBytes);
       if (e != cudaSuccess) return e;
-      e = launch_programmatic(gemm_tc_kernel<128>, units, Cfg<128, 1>::kSmemBytes, p, stream);
+      e = launch_programmatic(gemm_tc_kernel<128>, units, Cfg<128, 1>::kThreads, Cfg<128, 1>::kSmemBytes, p, stream);
       break;
   }
   if (e != cudaSuccess) return e;
