@@ -149,3 +149,55 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
         dm.version()
     with pytest.raises(dm.LibraryNotBuilt):
         dm.set_workspace_limit(0)
+
+
+C_CLIENT = r"""
+#include <stdio.h>
+#include <string.h>
+
+#include "dmuon.h"
+
+int main(void) {
+  float coeffs[15];
+  const int restarts[1] = {2};
+  const int64_t rows[3] = {14336, 4096, 1024};
+  const int64_t cols[3] = {4096, 4096, 4096};
+  int owner[3];
+  double loads[2];
+  size_t bytes = 0;
+  int i, rc;
+  for (i = 0; i < 15; ++i) coeffs[i] = 1.0f;
+  if (strncmp(dmuon_version(), "dmuon-gb300", 11) != 0) return 1;
+  rc = dmuon_ns(NULL, 4, 8, coeffs, 5, restarts, 1, DMUON_NS_GRAM, 1e-7f, NULL);
+  if (rc != DMUON_ERR_INVALID_ARG || strstr(dmuon_last_error(), "NULL") == NULL) return 2;
+  rc = dmuon_assign_owners(3, rows, cols, NULL, 2, DMUON_COST_GRAM_FLOPS, owner, loads);
+  if (rc != DMUON_OK) return 3;
+  rc = dmuon_workspace_size(3, rows, cols, DMUON_NS_GRAM, &bytes);
+  if (rc != DMUON_OK || bytes == 0) return 4;
+  printf("%d %d %d %.17g %.17g %zu\n", owner[0], owner[1], owner[2], loads[0], loads[1], bytes);
+  return 0;
+}
+"""
+
+
+def test_header_serves_a_plain_c_client(L, tmp_path):
+    """include/dmuon.h compiles as strict C99 and a C program links libdmuon.so directly: the host-only
+    entry points (version, argument validation, owner assignment, workspace query) answer as they do
+    through the Python binding."""
+    import shutil
+
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "client.c"
+    src.write_text(C_CLIENT)
+    exe = tmp_path / "client"
+    libdir = os.path.dirname(dm.LIB_PATH)
+    subprocess.run([cc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror", "-I", os.path.join(ROOT, "include"),
+                    str(src), "-L", libdir, "-ldmuon", f"-Wl,-rpath,{libdir}", "-o", str(exe)], check=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split()
+    shapes = [(14336, 4096), (4096, 4096), (1024, 4096)]
+    owners, loads = dm.assign_owners(shapes, 2, None, "gram_flops")
+    assert [int(v) for v in out[:3]] == list(owners)
+    assert [float(v) for v in out[3:5]] == list(loads)
+    assert int(out[5]) == dm.workspace_size(shapes, "gram")
