@@ -552,9 +552,14 @@ __global__ void __launch_bounds__(kSmallThreads, 1) ns_small_kernel(const __grid
   bad |= __hisnan(__low2half(chk16)) || __hisnan(__high2half(chk16)) || chk32 != chk32;
   if (bad) atomicOr(p.status, kDevNonfinite);
   // After an abort, let any copy or MMA still in flight finish before shared and tensor memory go away.
+  // Every thread waited once per product, so the last product's phase has parity mma_phase ^ 1 and may
+  // still be pending; the drain commit completes the phase after it. A wait on the drain's parity alone
+  // would return at once while the product's phase is open (it names the completed phase before), so
+  // both phases are waited for, in order.
   if (*abort_flag) {
     if (tid == 0) {
       mma_commit(&bar_mma[1]);
+      wait_bounded(&bar_mma[1], mma_phase ^ 1u, abort_flag, p.status, kDrainLimitNs, false);
       wait_bounded(&bar_mma[1], mma_phase, abort_flag, p.status, kDrainLimitNs, false);
     }
   }
