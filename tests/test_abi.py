@@ -134,6 +134,18 @@ def test_workspace_size_closed_form(L):
     assert small <= got <= small * 1.001 + (1 << 22)
 
 
+def test_workspace_size_of_fused_small_plans(L):
+    """A call whose every matrix has m <= 128 and n <= 512 runs the fused small-matrix kernel, which keeps
+    X, R, Z and Q in shared memory: its workspace is tables only. One larger matrix sends the whole call to
+    the grouped path, which needs the per-matrix buffers again."""
+    small = [(128, 512)] * 50 + [(512, 128)] * 50
+    for backend in ("gram", "direct", "auto"):
+        assert dm.workspace_size(small, backend) < 100 * 1024
+    mixed = small[:-1] + [(129, 512)]
+    gram = sum(2 * 2 * min(s) * (-(-max(s) // 8) * 8) + 5 * 2 * min(s) * (-(-min(s) // 8) * 8) for s in mixed)
+    assert gram <= dm.workspace_size(mixed, "gram") <= gram * 1.001 + (1 << 22)
+
+
 def test_oversized_dimension_rejected(L):
     c = (ctypes.c_float * 15)(*[1.0] * 15)
     r = (ctypes.c_int * 1)(2)
