@@ -4,15 +4,22 @@ A step is the whole path on every matrix: momentum accumulate (bf16 gradients, f
 Frobenius normalisation, fp16 cast, five Newton-Schulz steps (Gram form with restart [2] by default,
 POLAR_EXPRESS coefficients) and the fp32 weight update -- one dmuon_muon_step call.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--backend gram|direct] [--layers L]
-    python bench.py --impl reference ...   # the CPU float64 oracle on a bounded sample
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--backend gram|direct] [--layers L] [--owned]
+    python bench.py --impl reference ...   # the CPU float64 oracle, timed per matrix and extrapolated
 
-value = algorithmic Newton-Schulz TFLOP/s of the whole job (every symmetric product counted at half:
-Gram as implemented 6 m^2 n + 17 m^3 per matrix -- R, Z and S = (aI+Z)R are symmetric, Q is a full
-product --, direct 15 m^2 n + 5 m^3) over the device-timed region, inputs resident in HBM. Every input is larger than L2 (129 MB) except the small Gram matrices, so no flush is inserted.
+value = algorithmic Newton-Schulz TFLOP/s of the whole job over the device-timed region, inputs resident
+in HBM: Gram 6 m^2 n + 20 m^3 per matrix (the symmetric products X X^T, R^2 and R = S (aI+Z) counted at
+half, S = (aI+Z) R as the full product the method writes), direct 15 m^2 n + 5 m^3. The library computes
+S as a symmetric product too (it is one in exact arithmetic), so it executes 6 m^2 n + 17 m^3; the line
+reports that count under "as_executed". Every input is larger than L2 (129 MB) except the small Gram
+matrices, so no flush is inserted.
 e2e = the same metric through the public call a caller with host gradients makes
 (dmuon_muon_step_host: the step's gradients copied in from pinned host memory inside the call, the copies
 pipelined against the computation) and the per-matrix norms read back, inside the timed region.
+configs = the other configurations, each timed on its own with CUDA events and its own clock record:
+the single 256 x 1024 matrix (both forms), the closed-form 4096 x 4096 and 2048 x 8192 matrices through
+dmuon_ns (both forms), the 2560 small matrices in one grouped step, and the whole Llama-3-8B set in the
+direct form.
 """
 
 from __future__ import annotations
@@ -34,7 +41,7 @@ UNIT = "TFLOP/s"
 LR, BETA, EPS = 0.02, 0.95, 1e-7
 
 
-def parse():
+def parse(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
@@ -45,16 +52,23 @@ def parse():
     ap.add_argument("--layers", type=int, default=32)
     ap.add_argument("--workload", default="llama", choices=["llama", "small", "adamw", "ns-configs"],
                     help="llama: Llama-3-8B Muon-target set (the headline); small: 2048 x 128x512 + 512 x 512x128; "
-                         "adamw: AdamW over the Llama-3-8B non-Muon parameters; ns-configs: the single "
-                         "256x1024 matrix and the closed-form 4096^2 and 2048x8192 dmuon_ns cases, both forms")
+                         "adamw: AdamW over the Llama-3-8B non-Muon parameters; ns-configs: only the other "
+                         "configurations (the single 256x1024 matrix, the closed-form dmuon_ns cases, the small "
+                         "set, the 8B set in the direct form)")
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--e2e-groups", type=int, default=0,
                     help="pipeline groups of the host-gradient call (0: the library's choice, 1: no overlap)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline (profiling runs)")
+    ap.add_argument("--config-steps", type=int, default=10,
+                    help="timed calls per other configuration (0: skip them)")
+    ap.add_argument("--owned", action="store_true",
+                    help="dedicated ownership across the ranks: each rank updates only the matrices "
+                         "dmuon_assign_owners gives it (LPT over Gram flops, same-layer spread), so the job "
+                         "is one matrix set (strong scaling) instead of one per rank")
     ap.add_argument("--torch-mm-context", action="store_true",
                     help="time the same step written with torch.mm (cuBLAS) instead; context only")
-    return ap.parse_args()
+    return ap.parse_args(argv)
 
 
 def workload_config(args):
@@ -85,13 +99,29 @@ def restart_list(args):
     return tuple(int(x) for x in args.restarts.split(",") if x.strip() != "")
 
 
-def total_flops(shapes, backend, restarts=(2,), dense=False):
+def matrix_flops(r, c, backend, restarts=(2,), dense=False, as_executed=False):
+    """Newton-Schulz flops of one matrix: the algorithmic count (Gram 6 m^2 n + 20 m^3 with the defaults,
+    S = (aI+Z) R a full product), or with as_executed the library's (S symmetric: 6 m^2 n + 17 m^3);
+    dense counts every symmetric product in full."""
     import newton_schulz_momentum_gb300 as dm
+    direct = backend == "direct" or (backend == "auto" and dm.auto_uses_direct(r, c))
+    if direct:
+        return dm.direct_flops(r, c, dense=dense)
+    return dm.gram_flops(r, c, 5, restarts, dense=dense, s_symmetric=as_executed)
 
-    def one(r, c):
-        direct = backend == "direct" or (backend == "auto" and dm.auto_uses_direct(r, c))
-        return dm.direct_flops(r, c, dense=dense) if direct else dm.gram_flops(r, c, 5, restarts, dense=dense)
-    return sum(one(r, c) for _, r, c in shapes)
+
+def total_flops(shapes, backend, restarts=(2,), dense=False, as_executed=False):
+    """matrix_flops summed over one step's matrices."""
+    return sum(matrix_flops(r, c, backend, restarts, dense, as_executed) for _, r, c in shapes)
+
+
+def owned_shapes(shapes, world, rank):
+    """The matrices rank `rank` owns when `world` ranks split the set by dedicated ownership (LPT over
+    Gram flops with the same-layer spread rule, computed identically on every rank)."""
+    import newton_schulz_momentum_gb300 as dm
+    layer_of = [int(name.split(".")[1]) if name.startswith("layers.") else 0 for name, _, _ in shapes]
+    owners, _ = dm.assign_owners([(r, c) for _, r, c in shapes], world, layer_of, "gram_flops")
+    return [s for s, o in zip(shapes, owners) if o == rank]
 
 
 # The GEMM's DRAM traffic depends on the kernel and on the planner's tile order.
@@ -187,42 +217,6 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def cpu_oracle_sample(shapes, backend, seconds, seed=7, small=False):
-    """Time the float64 oracle (as it stands) on whole matrices of the workload's distinct oriented
-    shapes, cycling until about `seconds` of CPU work. Returns (TFLOP/s, flops, seconds, sample text)."""
-    import numpy as np
-
-    import newton_schulz_momentum_gb300 as dm
-    import workloads
-    from oracle import ns64
-
-    distinct = []
-    for name, r, c in shapes:
-        key = (min(r, c), max(r, c))
-        if key not in [(min(a, b), max(a, b)) for _, a, b in distinct]:
-            distinct.append((name, r, c))
-    distinct.sort(key=lambda t: t[1] * t[2])
-    flops, spent, done = 0, 0.0, []
-    i = 0
-    while spent < seconds or not done:
-        name, r, c = distinct[i % len(distinct)]
-        g = workloads.gaussian((r, c), 1e-3, seed + i)
-        if not small:
-            g = workloads.round_to_bf16(g)[0]
-        w = workloads.gaussian((r, c), 0.02, seed + 100 + i)
-        m0 = np.zeros((r, c), dtype=np.float32)
-        coeffs = ns64.YOU if small else ns64.POLAR_EXPRESS
-        t0 = time.perf_counter()
-        ns64.muon_step(w, g, m0, LR, BETA, coeffs, (2,) if backend == "gram" else (), backend, EPS)
-        spent += time.perf_counter() - t0
-        flops += (dm.gram_flops if backend == "gram" else dm.direct_flops)(r, c)
-        done.append(f"{name.split('.')[-1]} {r}x{c}")
-        i += 1
-        if i >= 3 * len(distinct) and not small:
-            break
-    return flops / spent / 1e12, flops, spent, "whole-matrix oracle Muon steps: " + ", ".join(done)
-
-
 def host_cores():
     try:
         return len(os.sched_getaffinity(0))
@@ -230,30 +224,129 @@ def host_cores():
         return os.cpu_count() or 1
 
 
+def cpu_info():
+    """The host CPU's model name and the BLAS library NumPy uses (what the oracle's matrix products run on)."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.strip().startswith("Model name:"):
+                model = ln.split(":", 1)[1].strip()
+                break
+    except Exception:
+        pass
+    if not model:
+        try:
+            with open("/proc/cpuinfo") as fh:
+                for ln in fh:
+                    if ln.lower().startswith(("model name", "cpu model")):
+                        model = ln.split(":", 1)[1].strip()
+                        break
+        except Exception:
+            pass
+    import numpy as np
+    blas = None
+    try:
+        deps = np.show_config(mode="dicts")["Build Dependencies"]
+        b = deps.get("blas", {})
+        blas = " ".join(str(b.get(k)) for k in ("name", "version") if b.get(k)) or None
+    except Exception:
+        pass
+    return {"cpu_model": model, "blas": blas, "numpy": np.__version__}
+
+
+def distinct_oriented(shapes):
+    """[(rows, cols, count)]: one stored shape per distinct oriented shape (min, max), with how many of the
+    workload's matrices have it, smallest first."""
+    seen = {}
+    for _, r, c in shapes:
+        key = (min(r, c), max(r, c))
+        if key not in seen:
+            seen[key] = [r, c, 0]
+        seen[key][2] += 1
+    return sorted((tuple(v) for v in seen.values()), key=lambda t: t[0] * t[1])
+
+
+def oracle_matrix_seconds(r, c, backend, small, seed):
+    """Wall time of one oracle Muon step (float64 NumPy, as it stands) on one whole r x c matrix of the
+    workload's distribution."""
+    import numpy as np
+
+    import workloads
+    from oracle import ns64
+    g = workloads.gaussian((r, c), 1e-3, seed)
+    if not small:
+        g = workloads.round_to_bf16(g)[0]
+    w = workloads.gaussian((r, c), 0.02, seed + 100)
+    m0 = np.zeros((r, c), dtype=np.float32)
+    coeffs = ns64.YOU if small else ns64.POLAR_EXPRESS
+    t0 = time.perf_counter()
+    ns64.muon_step(w, g, m0, LR, BETA, coeffs, (2,) if backend == "gram" else (), backend, EPS)
+    return time.perf_counter() - t0
+
+
+def cpu_oracle_sample(shapes, backend, seconds, seed=7, small=False):
+    """Time the float64 oracle on whole matrices of the workload's distinct oriented shapes (smallest
+    first, cycling) until about `seconds` of CPU work. Returns (TFLOP/s on the algorithmic count, flops,
+    seconds, sample text)."""
+    distinct = distinct_oriented(shapes)
+    flops, spent, done = 0, 0.0, []
+    i = 0
+    while spent < seconds or not done:
+        r, c, _ = distinct[i % len(distinct)]
+        spent += oracle_matrix_seconds(r, c, backend, small, seed + i)
+        flops += matrix_flops(r, c, backend)
+        done.append(f"{r}x{c}")
+        i += 1
+        if i >= 3 * len(distinct):
+            break
+    return flops / spent / 1e12, flops, spent, "whole-matrix oracle Muon steps: " + ", ".join(done)
+
+
 def run_reference(args):
-    """--impl reference: the CPU float64 oracle on the same workload, metric and unit."""
+    """--impl reference: the CPU float64 oracle (as it stands) on the same workload, metric and unit. Each
+    timed step is one whole-matrix oracle Muon step, taking the workload's distinct oriented shapes in
+    turn; the full step's time is extrapolated as the sum over the distinct shapes of (matrices of that
+    shape x the mean measured time per matrix), since the whole 224-matrix step would take about twenty
+    minutes of CPU time. value = the full step's algorithmic flops / that extrapolated time."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
     shapes, cfg = workload_config(args)
-    per_step = max(args.cpu_seconds / 4.0, 1.0)
-    for _ in range(args.warmup):
-        cpu_oracle_sample(shapes[:7], args.backend, 0.0, small=args.workload == "small")
-    tflops, flops, secs = [], 0, 0.0
-    sample = ""
-    for _ in range(args.steps):
-        v, f, s, sample = cpu_oracle_sample(shapes[:7], args.backend, per_step, small=args.workload == "small")
-        tflops.append(v)
-        flops += f
-        secs += s
-    value = flops / secs / 1e12
+    small = args.workload == "small"
+    distinct = distinct_oriented(shapes)
+    for i in range(args.warmup):
+        oracle_matrix_seconds(distinct[0][0], distinct[0][1], args.backend, small, 11 + i)
+    per_shape = {}
+    wall = []
+    for i in range(args.steps):
+        r, c, _ = distinct[i % len(distinct)]
+        t = oracle_matrix_seconds(r, c, args.backend, small, 21 + i)
+        per_shape.setdefault((r, c), []).append(t)
+        wall.append(t)
+    sampled_flops = sum(matrix_flops(r, c, args.backend) * len(ts) for (r, c), ts in per_shape.items())
+    rate = sampled_flops / sum(wall)  # flop/s over the sample, for shapes the sample did not reach
+    step_s = 0.0
+    for r, c, count in distinct:
+        ts = per_shape.get((r, c))
+        step_s += count * (statistics.mean(ts) if ts else matrix_flops(r, c, args.backend) / rate)
+    flops_step = total_flops(shapes, args.backend)
+    value = flops_step / step_s / 1e12
+    sample = (f"{args.steps} whole-matrix oracle Muon steps, one per timed step, cycling the distinct oriented "
+              f"shapes ({', '.join(f'{r}x{c}: {len(per_shape.get((r, c), []))}' for r, c, _ in distinct)}); "
+              f"float64 NumPy")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * step_s,
+        "ms_per_step_kind": "extrapolated: sum over the distinct shapes of matrices x mean measured oracle time "
+                            "per matrix",
+        "sample_ms_per_step": 1e3 * statistics.mean(wall),
+        "per_shape_s": {f"{r}x{c}": {"matrices": count, "mean_s": statistics.mean(per_shape[(r, c)])
+                                      if (r, c) in per_shape else None} for r, c, count in distinct},
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": cfg,
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
-                         "sample": f"per step about {per_step:.0f} s of {sample}"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": host_cores(), "kind": "oracle", "sample": sample,
+                         **cpu_info()},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -361,6 +454,157 @@ def run_e2e(args, G, norms, make_host_step, barrier, stream, world, flops_step):
             "h2d_copy_ms_this_box": link_ms}
 
 
+def time_calls(fn, stream, dev, steps, prep=None):
+    """CUDA-event times (ms) of `steps` calls of fn on `stream`, each bracketed by its own events (prep, if
+    given, is enqueued before the start event and not timed): median, p90 and min."""
+    import torch
+    marks = []
+    for _ in range(steps):
+        if prep is not None:
+            prep()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        marks.append((a, b))
+    torch.cuda.synchronize(dev)
+    ms = sorted(a.elapsed_time(b) for a, b in marks)
+    return {"ms_median": statistics.median(ms), "ms_p90": ms[min(len(ms) - 1, int(0.9 * len(ms)))],
+            "ms_min": ms[0], "calls": len(ms)}
+
+
+def closed_form_on_device(m, n, sigma, seed, dev):
+    """X = U diag(sigma) V^T as fp32 on the device, U (m x k) and V (n x k) orthonormal from the QR of seeded
+    float64 Gaussians, k = min(m, n): the distribution of the closed-form parity cases, drawn on the GPU
+    because NumPy's QR takes tens of seconds at these sizes (input generation only)."""
+    import torch
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(seed)
+    k = min(m, n)
+
+    def orth(rows):
+        q, r = torch.linalg.qr(torch.randn((rows, k), generator=gen, device=dev, dtype=torch.float64))
+        return q * torch.sign(torch.diagonal(r))
+    u, v = orth(m), orth(n)
+    s = torch.as_tensor(sigma, dtype=torch.float64, device=dev)
+    return ((u * s) @ v.T).float().contiguous()
+
+
+def run_configs(args, dev, local, big=None):
+    """The configurations beside the headline, one at a time, each with a clock record: CUDA events around
+    every call on the current stream, --config-steps timed calls after max(--warmup, 3) untimed ones.
+      * Llama-3-8B set in the direct form (big = (shapes, W, G, M) of the headline, same buffers);
+      * the 2560 small matrices (2048 x 128x512 + 512 x 512x128, fp32 N(0, 1e-3^2) gradients, YOU, Gram
+        restart [2]) in one grouped step; HBM-bound: 20 B per element at least (G, M in; M out; W in and
+        out), 24 B moved (the momentum pass, then the fused kernel reads M once more);
+      * the single 256 x 1024 Muon step (fp32 N(0, 1) gradient, YOU), both forms; latency-bound;
+      * dmuon_ns on the closed-form 4096 x 4096 matrix (singular values log-uniform in [1e-6, 1]) and
+        2048 x 8192 matrix (205 singular values 1, the rest 1e-4), POLAR_EXPRESS, both forms; each call
+        starts from a fresh copy of the input made before its start event.
+    Flop rates use the algorithmic counts (Gram 6 m^2 n + 20 m^3 with restart [2], direct 15 m^2 n + 5 m^3)."""
+    import torch
+
+    import newton_schulz_momentum_gb300 as dm
+    import workloads
+
+    hbm, tc_burst, tc_sust, src = peaks()
+    stream = torch.cuda.current_stream(dev)
+    cs = stream.cuda_stream
+    n = args.config_steps
+    warm = max(args.warmup, 3)
+    out = {"timing": f"CUDA events per call, median of {n} after {warm} untimed calls; peaks {src}"}
+
+    def run(fn, prep=None, timing=False):
+        for _ in range(warm):
+            if prep is not None:
+                prep()
+            fn()
+        dm.check_status(stream)
+        if timing:
+            dm.timing_enable(True)
+        with ClockSampler(local) as clk:
+            t = time_calls(fn, stream, dev, n, prep)
+        kt = None
+        if timing:
+            kt = dm.timing_read()
+            dm.timing_enable(False)
+        dm.check_status(stream)
+        t["clocks"] = clk.summary()
+        return t, kt
+
+    if big is not None:
+        shapes, W, G, M = big
+        step = dm.MuonStep(W, G, M, coeffs=dm.POLAR_EXPRESS, restarts=(), backend="direct", eps=EPS)
+        t, kt = run(lambda: step(lr=LR, beta=BETA, stream=cs), timing=True)
+        flops = total_flops(shapes, "direct")
+        gms, gn = kt["gemm_tc"]
+        t.update({"config": "whole Llama-3-8B Muon-target set (224 matrices), bf16 grads, direct form, POLAR_EXPRESS",
+                  "tflops": flops / (t["ms_median"] * 1e-3) / 1e12, "tflop_per_step": flops / 1e12,
+                  "frac_of_sustained_peak": flops / (t["ms_median"] * 1e-3) / 1e12 / tc_sust,
+                  "gemm_tc_ms_per_step": gms / n, "gemm_tc_launches_per_step": gn / n,
+                  "gemm_tc_tflops": flops * n / (gms * 1e-3) / 1e12 if gms > 0 else None})
+        out["llama3_8b_direct"] = t
+        del step
+
+    # ---- the small-matrix set, one grouped step
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(4)
+    sshapes = workloads.small_set_shapes()
+    W = [torch.randn(s, generator=gen, device=dev) * 0.02 for s in sshapes]
+    G = [torch.randn(s, generator=gen, device=dev) * 1e-3 for s in sshapes]
+    M = [torch.zeros(s, device=dev) for s in sshapes]
+    step = dm.MuonStep(W, G, M, coeffs=dm.YOU, restarts=(2,), backend="gram", eps=EPS)
+    t, kt = run(lambda: step(lr=LR, beta=BETA, stream=cs), timing=True)
+    elems = sum(r * c for r, c in sshapes)
+    flops = sum(matrix_flops(r, c, "gram") for r, c in sshapes)
+    sec = t["ms_median"] * 1e-3
+    t.update({"config": "2048 x 128x512 + 512 x 512x128 fp32 grads N(0, 1e-3^2), YOU, Gram restart [2], one grouped step",
+              "elements": elems, "tflops": flops / sec / 1e12,
+              "bytes_moved_per_step": 24 * elems, "gbs_moved": 24 * elems / sec / 1e9,
+              "bytes_algorithmic_per_step": 20 * elems, "gbs_algorithmic": 20 * elems / sec / 1e9,
+              "frac_of_hbm_algorithmic": 20 * elems / sec / 1e9 / hbm,
+              "roofline_ms": max(20 * elems / (hbm * 1e9), flops / (tc_sust * 1e12)) * 1e3,
+              "kernel_ms_per_step": {k: v[0] / n for k, v in kt.items() if v[1]},
+              "launches_per_step": {k: v[1] / n for k, v in kt.items() if v[1]}})
+    out["small_set_2560"] = t
+    del step, W, G, M
+
+    # ---- one 256 x 1024 matrix, the whole Muon step, both forms
+    g = torch.from_numpy(workloads.gaussian((256, 1024), 1.0, 1)).to(dev)
+    for backend in ("gram", "direct"):
+        W1 = [torch.from_numpy(workloads.gaussian((256, 1024), 0.02, 2)).to(dev)]
+        M1 = [torch.zeros((256, 1024), device=dev)]
+        step = dm.MuonStep(W1, [g], M1, coeffs=dm.YOU, restarts=(2,), backend=backend, eps=EPS)
+        t, kt = run(lambda: step(lr=LR, beta=BETA, stream=cs), timing=True)
+        flops = matrix_flops(256, 1024, backend)
+        t.update({"config": "single 256x1024 Muon step, fp32 N(0, 1) gradient, YOU", "bound": "latency",
+                  "us_median": t["ms_median"] * 1e3, "tflops": flops / (t["ms_median"] * 1e-3) / 1e12,
+                  "launches_per_step": {k: v[1] / n for k, v in kt.items() if v[1]}})
+        out[f"single_256x1024_{backend}"] = t
+        del step
+
+    # ---- closed-form matrices through dmuon_ns
+    cases = (("closed_form_4096x4096", "4096x4096, sigma log-uniform in [1e-6, 1], POLAR_EXPRESS", 4096, 4096,
+              workloads.log_uniform_spectrum(4096, 1e-6, 1.0, 2), 2),
+             ("closed_form_2048x8192", "2048x8192, 205 sigma = 1, the rest 1e-4, POLAR_EXPRESS", 2048, 8192,
+              workloads.top_fraction_spectrum(2048, 0.1, 1.0, 1e-4), 3))
+    for key, name, m, nn, sigma, seed in cases:
+        x0 = closed_form_on_device(m, nn, sigma, seed, dev)
+        x = torch.empty_like(x0)
+        for backend in ("gram", "direct"):
+            t, kt = run(lambda: dm.ns(x, dm.POLAR_EXPRESS, (2,), backend, EPS, stream=cs),
+                        prep=lambda: x.copy_(x0), timing=True)
+            flops = matrix_flops(m, nn, backend)
+            tf = flops / (t["ms_median"] * 1e-3) / 1e12
+            t.update({"config": f"dmuon_ns {name}", "bound": "tensor", "tflops": tf,
+                      "frac_of_burst_peak": tf / tc_burst,
+                      "launches_per_call": {k: v[1] / n for k, v in kt.items() if v[1]}})
+            out[f"{key}_{backend}"] = t
+        del x0, x
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_native(args):
     import torch
     import torch.distributed as dist
@@ -379,8 +623,14 @@ def run_native(args):
     dmbuild.build()
     dm.lib()
 
-    shapes, cfg = workload_config(args)
-    flops_step = total_flops(shapes, args.backend, restart_list(args))
+    all_shapes, cfg = workload_config(args)
+    shapes = owned_shapes(all_shapes, world, rank) if args.owned else all_shapes
+    if args.owned:
+        cfg = dict(cfg, ownership=f"dedicated: {world} ranks, LPT over Gram flops (dmuon_assign_owners)")
+    restarts = restart_list(args)
+    flops_step = total_flops(shapes, args.backend, restarts)  # this rank's matrices
+    flops_job = total_flops(all_shapes, args.backend, restarts) if args.owned else world * flops_step
+    flops_exec = total_flops(shapes, args.backend, restarts, as_executed=True)
     dev = torch.device("cuda", local)
     gen = torch.Generator(device=dev)
     gen.manual_seed(1234 + rank)
@@ -394,15 +644,14 @@ def run_native(args):
     norms = torch.empty(len(shapes), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    muon = dm.MuonStep(W, G, M, coeffs=coeffs, restarts=restart_list(args), backend=args.backend, eps=EPS,
-                       norms_out=norms)
+    muon = dm.MuonStep(W, G, M, coeffs=coeffs, restarts=restarts, backend=args.backend, eps=EPS, norms_out=norms)
     cuda_stream = stream.cuda_stream
 
     def step():
         muon(lr=LR, beta=BETA, stream=cuda_stream)
 
     def make_host_step(host_grads):
-        host_muon = dm.MuonStep(W, G, M, coeffs=coeffs, restarts=restart_list(args), backend=args.backend, eps=EPS,
+        host_muon = dm.MuonStep(W, G, M, coeffs=coeffs, restarts=restarts, backend=args.backend, eps=EPS,
                                 norms_out=norms, host_grads=host_grads, groups=args.e2e_groups)
         return lambda: host_muon(lr=LR, beta=BETA, stream=cuda_stream)
 
@@ -434,7 +683,7 @@ def run_native(args):
     dm.check_status(stream)
     exec_flops, exec_tiles, _ = dm.plan_info()
     ms_step = max_over_ranks(start.elapsed_time(stop), dev) / args.steps
-    value = whole_job_tflops(flops_step, world, ms_step)
+    value = flops_job / (ms_step * 1e-3) / 1e12
     per_step = sorted(marks[i].elapsed_time(marks[i + 1]) for i in range(args.steps))
     kernel_times = {c: (sum(ms for k, ms in launch_list if k == c), sum(1 for k, _ in launch_list if k == c))
                     for c in dm.TIMING_CLASSES}
@@ -449,6 +698,8 @@ def run_native(args):
     e2e = None
     if args.e2e_steps > 0:
         e2e = run_e2e(args, G, norms, make_host_step, barrier, stream, world, flops_step)
+        if args.owned:
+            e2e["value"] = flops_job / (e2e["ms_per_step"] * 1e-3) / 1e12
 
     # ---- roofline of the dominant kernel (the tensor-core GEMM), from the live events
     hbm, tc_burst, tc_sust, src = peaks()
@@ -458,29 +709,41 @@ def run_native(args):
     launches = sum(n for _, n in kernel_times.values())
     rw_ms = sum(kernel_times[k][0] for k in ("momentum_sumsq", "finalize_norms", "normalize_cast"))
     # momentum: G (2 B bf16 / 4 B fp32) + M read 4 + M write 4; normalise: M read 4 + X write 2 (no
-    # separate normalise pass when the fused small-matrix kernel reads M itself)
+    # separate normalise pass when the fused small-matrix kernel reads M itself). The algorithmic minimum
+    # reads G and M once and writes M and X once: 12 B (bf16 G) or 14 B (fp32 G) per element.
     fused_small = kernel_times["normalize_cast"][1] == 0
-    rw_bytes = (2 if gdtype == torch.bfloat16 else 4) + 4 + 4 + (0 if fused_small else 4 + 2)
+    gsize = 2 if gdtype == torch.bfloat16 else 4
+    rw_bytes = gsize + 4 + 4 + (0 if fused_small else 4 + 2)
+    rw_alg = gsize + 4 + 4 + 2
+    elems = sum(r * c for _, r, c in shapes)
 
     # dedicated ownership of this matrix set over 8 owner ranks (host-only LPT), timed and its balance
-    layer_of = [int(name.split(".")[1]) if name.startswith("layers.") else 0 for name, _, _ in shapes]
+    layer_of = [int(name.split(".")[1]) if name.startswith("layers.") else 0 for name, _, _ in all_shapes]
     t0 = time.perf_counter()
-    _, loads = dm.assign_owners([(r, c) for _, r, c in shapes], 8, layer_of, "gram_flops")
+    _, loads = dm.assign_owners([(r, c) for _, r, c in all_shapes], 8, layer_of, "gram_flops")
     owner_us = (time.perf_counter() - t0) * 1e6
     ownership = {"ranks": 8, "cost": "gram_flops", "max_over_mean_load": max(loads) / (sum(loads) / 8),
                  "host_us": owner_us}
+
+    # ---- the other configurations (one GPU only), then the CPU oracle baseline
+    configs = None
+    if world == 1 and args.config_steps > 0:
+        configs = run_configs(args, dev, local, (shapes, W, G, M) if args.workload == "llama" else None)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
         v, f, s, sample = cpu_oracle_sample(shapes, args.backend, args.cpu_seconds, small=args.workload == "small")
         cpu = {"value": v, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
-               "sample": f"{sample} ({f / 1e12:.2f} TFLOP in {s:.1f} s, float64 NumPy)"}
+               "sample": f"{sample} ({f / 1e12:.2f} TFLOP in {s:.1f} s, float64 NumPy)", **cpu_info()}
 
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f16", "data": "synthetic", "config": cfg,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+            "scaling": "strong" if args.owned else "weak", "vs_baseline": None, "dtype": "f16",
+            "data": "synthetic", "config": cfg,
+            "flop_count": ("algorithmic: Gram 6 m^2 n + 20 m^3 per matrix (symmetric products at half, "
+                           "S = (aI+Z) R in full), direct 15 m^2 n + 5 m^3"),
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": tc_sust, "unit": "TFLOP/s",
                          "frac": (achieved / tc_sust) if achieved else None,
                          "traffic": measured_traffic(cfg["workload"], args.backend),
@@ -492,24 +755,32 @@ def run_native(args):
             "e2e": e2e,
             "gpu_launches": launches,
             "clocks": clocks.summary(),
+            "as_executed": {"count": "Gram 6 m^2 n + 17 m^3 (S symmetric, as the library computes it)",
+                            "tflop_per_step": flops_exec / 1e12,
+                            "tflops": flops_exec * (flops_job / flops_step) / (ms_step * 1e-3) / 1e12,
+                            "gemm_tflops": flops_exec * args.steps / (gemm_ms * 1e-3) / 1e12 if gemm_ms > 0 else None,
+                            "gemm_frac_of_sustained_peak": flops_exec * args.steps / (gemm_ms * 1e-3) / 1e12 / tc_sust
+                            if gemm_ms > 0 else None},
             "breakdown_ms_per_step": {k: v[0] / args.steps for k, v in kernel_times.items()},
             "launches_per_step": {k: v[1] / args.steps for k, v in kernel_times.items()},
-            "rowwise_hbm": {"bytes_per_step": sum(r * c for _, r, c in shapes) * rw_bytes,
-                            "achieved_gbs": (sum(r * c for _, r, c in shapes) * rw_bytes * args.steps / (rw_ms * 1e-3) / 1e9)
-                            if rw_ms > 0 else None, "peak_gbs": hbm,
-                            "copy_gbs_this_box": live_copy_gbs},
+            "rowwise_hbm": {"bytes_per_step": elems * rw_bytes,
+                            "achieved_gbs": elems * rw_bytes * args.steps / (rw_ms * 1e-3) / 1e9 if rw_ms > 0 else None,
+                            "algorithmic_bytes_per_step": elems * rw_alg,
+                            "algorithmic_gbs": elems * rw_alg * args.steps / (rw_ms * 1e-3) / 1e9 if rw_ms > 0 else None,
+                            "peak_gbs": hbm, "copy_gbs_this_box": live_copy_gbs},
             "ns_tflops_frac_of_peak": value / world / tc_sust,
             "step_ms": {"p50": statistics.median(per_step), "p90": per_step[min(len(per_step) - 1,
                                                                              int(0.9 * len(per_step)))],
                         "min": per_step[0], "max": per_step[-1]},
             "phases_ms_p50": phases,
-            "dense_tflops": whole_job_tflops(total_flops(shapes, args.backend, restart_list(args), dense=True),
-                                             world, ms_step),
+            "dense_tflops": (total_flops(shapes, args.backend, restarts, dense=True) * (flops_job / flops_step)
+                             / (ms_step * 1e-3) / 1e12),
             "executed": ({"tflop_per_step": exec_flops / 1e12, "tiles_per_step": exec_tiles,
                           "gemm_tflops": exec_flops * args.steps / (gemm_ms * 1e-3) / 1e12,
                           "frac_of_peak": exec_flops * args.steps / (gemm_ms * 1e-3) / 1e12 / tc_sust}
                          if exec_flops > 0 and gemm_ms > 0 else None),
             "owner_assignment": ownership,
+            "configs": configs,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -631,79 +902,16 @@ def run_torch_mm_context(args):
 
 
 def run_ns_configs(args):
-    """The configurations beside the headline, timed one call at a time (CUDA events around each call on
-    the current stream, median over --steps after --warmup): the single 256 x 1024 matrix (one Muon
-    step, fp32 N(0, 1) gradient, YOU; latency-bound, reported in microseconds) and dmuon_ns on the
-    closed-form 4096 x 4096 matrix (singular values log-uniform in [1e-6, 1]) and 2048 x 8192 matrix (205
-    singular values 1, the rest 1e-4) with POLAR_EXPRESS, each in the Gram form (restart [2]) and the
-    direct form; the 2048 x 8192 case also through dmuon_ns_tp split into 2 and 8 column shards. dmuon_ns
-    works in place, so each call starts from a fresh copy of the input, made before
-    its start event. Prints one JSON line."""
-    import statistics
-
-    import numpy as np
+    """--workload ns-configs: only the other configurations (run_configs), without the headline step;
+    prints one JSON line."""
     import torch
 
-    import newton_schulz_momentum_gb300 as dm
-    import workloads
-
+    from newton_schulz_momentum_gb300 import build as dmbuild
+    dmbuild.build()
     dev = torch.device("cuda", 0)
-    _, tc_burst, _, src = peaks()
-
-    def timeit(fn, prep=None):
-        marks = []
-        for i in range(args.warmup + args.steps):
-            if prep is not None:
-                prep()
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record()
-            fn()
-            b.record()
-            if i >= args.warmup:
-                marks.append((a, b))
-        torch.cuda.synchronize(dev)
-        ms = [a.elapsed_time(b) for a, b in marks]
-        return statistics.median(ms), min(ms)
-
-    out = []
-    g = torch.from_numpy(workloads.gaussian((256, 1024), 1.0, 1)).to(dev)
-    for backend in ("gram", "direct"):
-        W, M = [torch.zeros((256, 1024), device=dev)], [torch.zeros((256, 1024), device=dev)]
-        step = dm.MuonStep(W, [g], M, coeffs=dm.YOU, restarts=(2,), backend=backend)
-        med, best = timeit(lambda: step(lr=LR, beta=BETA))
-        dm.check_status()
-        flops = dm.gram_flops(256, 1024) if backend == "gram" else dm.direct_flops(256, 1024)
-        out.append({"config": "single 256x1024, Muon step, fp32 grad, YOU", "backend": backend,
-                    "us_median": med * 1e3, "us_min": best * 1e3, "tflops": flops / (med * 1e-3) / 1e12,
-                    "bound": "latency"})
-    cases = (("4096x4096 closed form, sigma log-uniform in [1e-6, 1], POLAR_EXPRESS", 4096, 4096,
-              workloads.log_uniform_spectrum(4096, 1e-6, 1.0, 2), 2),
-             ("2048x8192 closed form, 205 sigma = 1, the rest 1e-4, POLAR_EXPRESS", 2048, 8192,
-              workloads.top_fraction_spectrum(2048, 0.1, 1.0, 1e-4), 3))
-    for name, m, n, sigma, seed in cases:
-        x0 = torch.from_numpy(workloads.closed_form_matrix(m, n, sigma, seed)[0].astype(np.float32)).to(dev)
-        x = torch.empty_like(x0)
-        for backend in ("gram", "direct"):
-            med, best = timeit(lambda: dm.ns(x, dm.POLAR_EXPRESS, (2,), backend), prep=lambda: x.copy_(x0))
-            dm.check_status()
-            flops = dm.gram_flops(m, n) if backend == "gram" else dm.direct_flops(m, n)
-            tf = flops / (med * 1e-3) / 1e12
-            out.append({"config": name, "backend": backend, "ms_median": med, "ms_min": best, "tflops": tf,
-                        "bound": "tensor", "frac_of_burst_peak": tf / tc_burst})
-        if m == 2048:
-            # The column-split (tensor-parallel exact) Gram form emulated on this GPU: every Gram formation is
-            # `shards` per-shard products written in fp32, then the fixed-order reduction.
-            for shards in (2, 8):
-                med, best = timeit(lambda: dm.ns_tp(x, shards, dm.POLAR_EXPRESS, (2,)), prep=lambda: x.copy_(x0))
-                dm.check_status()
-                tf = dm.gram_flops(m, n) / (med * 1e-3) / 1e12
-                out.append({"config": name, "backend": f"gram, {shards} column shards (dmuon_ns_tp)",
-                            "ms_median": med, "ms_min": best, "tflops": tf, "bound": "tensor",
-                            "frac_of_burst_peak": tf / tc_burst})
-    print(json.dumps({"impl": "native", "workload": "ns-configs", "steps": args.steps, "warmup": args.warmup,
-                      "dtype": "f16", "data": "synthetic", "peak_tflops_burst": tc_burst,
-                      "peak_source": f"{src} bf16 burst (fp16 dense rate equals bf16)", "results": out}),
-          flush=True)
+    torch.cuda.set_device(dev)
+    print(json.dumps({"impl": "native", "workload": "ns-configs", "dtype": "f16", "data": "synthetic",
+                      "configs": run_configs(args, dev, 0)}), flush=True)
 
 
 def main():

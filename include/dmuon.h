@@ -215,7 +215,9 @@ DMUON_API int dmuon_gemm_f16(int64_t M, int64_t N, int64_t K, const void* A, int
  *   rows*cols must not exceed DMUON_NOALLOC_MAX_ELEMS (2^28); larger matrices are rejected with
  *   DMUON_ERR_INVALID_ARG before anything is launched.
  * The first call on a device (with that device current) looks up the scratch's device address; make
- * that first call before any stream capture. All calls share the one scratch array and it keeps the
+ * that first call before any stream capture. The address is kept per device together with the CUDA
+ * context it belongs to; a call that finds a different context current on the device (for instance
+ * after cudaDeviceReset) looks it up again. All calls share the one scratch array and it keeps the
  * last call's contents (nothing in it needs to start at zero), so calls whose work overlaps on the GPU
  * race with each other: order them on one stream or synchronise between them.
  */

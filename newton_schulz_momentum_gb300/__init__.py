@@ -416,15 +416,21 @@ def release_workspace():
     _check(lib().dmuon_release_workspace())
 
 
-def gram_flops(m, n, steps=5, restarts=DEFAULT_RESTARTS, dense=False):
-    """Algorithmic flops of Gram NS as implemented, on one matrix (m <= n after orientation), every
-    symmetric product counted at half: X X^T m^2 n; per step R^2 m^3, the Q update Z Q 2 m^3 unless right
-    after a (re)start, the R update (S = (aI+Z) R and R = S (aI+Z), both symmetric) 2 m^3 when the next
-    step exists and is not a restart; restart Q X 2 m^2 n + X X^T m^2 n; output Q X 2 m^2 n. With the
-    default 5 steps and restart [2]: 6 m^2 n + 17 m^3. dense=True counts the symmetric products in full
-    (8 m^2 n + 28 m^3 with the defaults), the count a general GEMM would execute."""
+def gram_flops(m, n, steps=5, restarts=DEFAULT_RESTARTS, dense=False, s_symmetric=True):
+    """Flops of Gram NS on one matrix (m <= n after orientation), every symmetric product counted at half:
+    X X^T m^2 n; per step R^2 m^3, the Q update Z Q 2 m^3 unless right after a (re)start, the R update
+    R <- (aI+Z) R (aI+Z) when the next step exists and is not a restart; restart Q X 2 m^2 n + X X^T m^2 n;
+    output Q X 2 m^2 n.
+
+    The R update is S = (aI+Z) R followed by R = S (aI+Z) (symmetric, m^3). With s_symmetric=True (the
+    library's execution: S is also symmetric in exact arithmetic and computed as an upper triangle plus
+    mirror) S costs m^3, and the default 5 steps with restart [2] give 6 m^2 n + 17 m^3. With
+    s_symmetric=False S is counted as the full product it is written as (2 m^3), the algorithmic count of
+    the method as stated: 6 m^2 n + 20 m^3. dense=True counts every symmetric product in full (8 m^2 n +
+    28 m^3 with the defaults), the count a general GEMM would execute."""
     m, n = min(m, n), max(m, n)
     h = 2 if dense else 1  # symmetric products: half, or in full
+    hs = h if s_symmetric else 2
     rs = {k for k in restarts if 0 < k < steps}
     f, fresh = h * m * m * n, True
     for k in range(steps):
@@ -434,7 +440,7 @@ def gram_flops(m, n, steps=5, restarts=DEFAULT_RESTARTS, dense=False):
         f += h * m ** 3 + (0 if fresh else 2 * m ** 3)
         fresh = False
         if k + 1 < steps and (k + 1) not in rs:
-            f += 2 * h * m ** 3
+            f += (hs + h) * m ** 3
     return f + 2 * m * m * n
 
 

@@ -22,6 +22,8 @@
 #include <string>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "dmuon.h"
 #include "internal.h"
 
@@ -217,13 +219,21 @@ cudaEvent_t take_event() {
   return e;
 }
 
-// Records events around one launch when timing is on; otherwise just launches.
+// Names of the timing classes (dmuon.h), also the NVTX range names of their launches.
+const char* const kClassNames[DMUON_TIMING_CLASSES] = {"dmuon momentum_sumsq", "dmuon finalize_norms",
+                                                        "dmuon normalize_cast", "dmuon gemm_tc",
+                                                        "dmuon adamw",          "dmuon tp_reduce"};
+
+// Records events around one launch when timing is on (and an NVTX range around its host-side enqueue, for
+// a profiler's timeline); otherwise just launches.
 template <typename F>
 cudaError_t timed(int cls, cudaStream_t stream, F&& launch) {
   if (!g_timing) return launch();
   cudaEvent_t a = take_event(), b = take_event();
   if (a) cudaEventRecord(a, stream);
+  nvtxRangePushA(kClassNames[cls]);
   const cudaError_t e = launch();
+  nvtxRangePop();
   if (b) cudaEventRecord(b, stream);
   if (a && b) {
     g_timed.push_back({cls, a, b});
@@ -302,21 +312,16 @@ JobSpec make_job(int mat, int M, int N, int K, int recipe, int flags, size_t a, 
 // changes the fp16 result by under 2% of its error while saving a third of the R update. Q is left a full
 // product: it carries the accumulated iteration into the output, and mirroring its upper triangle drops
 // the (fp16-rounding-sized) commutator of the stored Z and Q, which measurably raised the error on the
-// hardest closed-form spectrum. DMUON_GRAM_SYM overrides the choice: "none", "s" (default), "q", "sq".
-void symmetric_sq(bool* s_sym, bool* q_sym) {
-  const char* env = getenv("DMUON_GRAM_SYM");
-  const std::string v = env ? env : "s";
-  *s_sym = v == "s" || v == "sq";
-  *q_sym = v == "q" || v == "sq";
-}
+// hardest closed-form spectrum (2048 x 8192 with 205 singular values at 1 and the rest at 1e-4) close to
+// the fp16 iteration's tolerance.
+constexpr bool kMirrorS = true;
+constexpr bool kMirrorQ = false;
 
 void build_gram_phases(Plan& pl, const std::vector<int>& restarts, int steps, const std::vector<int>& idx,
                        std::vector<std::vector<JobSpec>>& out, std::vector<int>& out_coef) {
   const int nm = static_cast<int>(pl.mats.size());
-  bool s_sym = false, q_sym = false;
-  symmetric_sq(&s_sym, &q_sym);
-  const int s_flag = s_sym ? kJobSymmetric : 0;
-  const int q_flag = q_sym ? kJobSymmetric : 0;
+  const int s_flag = kMirrorS ? kJobSymmetric : 0;
+  const int q_flag = kMirrorQ ? kJobSymmetric : 0;
   std::vector<char> is_restart(steps + 1, 0);
   for (int r : restarts)
     if (r > 0 && r < steps) is_restart[r] = 1;
@@ -467,12 +472,10 @@ void build_direct_phases(Plan& pl, int steps, const std::vector<int>& idx, std::
 
 // Tile configuration of a launch: 128 x 128 single-CTA tiles when every product is at most 128 wide;
 // 128 x 256 single-CTA tiles when every product has at most 128 rows (a 256-row pair tile would be half
-// empty); otherwise 256 x 256 tiles on CTA pairs (DMUON_GEMM_TILE=single selects 128 x 256 tiles).
+// empty); otherwise 256 x 256 tiles on CTA pairs.
 int pick_tile(int max_m, int max_n) {
   if (max_n <= 128) return kTileSingle128;
   if (max_m <= 128) return kTileSingle256;
-  const char* env = getenv("DMUON_GEMM_TILE");
-  if (env && strcmp(env, "single") == 0) return kTileSingle256;
   return kTilePair256;
 }
 
@@ -496,9 +499,7 @@ int launch_tile(const std::vector<JobSpec>& ph, int pair_units) {
   int max_m = 0, max_n = 0;
   for (const JobSpec& j : ph) max_m = std::max(max_m, j.M), max_n = std::max(max_n, j.N);
   const int tile = pick_tile(max_m, max_n);
-  const char* env = getenv("DMUON_GEMM_TILE");
-  if (tile == kTilePair256 && !(env && strcmp(env, "pair") == 0) && count_tiles(ph, kTilePair256) < pair_units)
-    return kTileSingle128;
+  if (tile == kTilePair256 && count_tiles(ph, kTilePair256) < pair_units) return kTileSingle128;
   return tile;
 }
 
@@ -550,11 +551,9 @@ int build_plan_host(Plan& pl, const PlanKey& key, const std::vector<const void*>
   pl.off_partials = lay.take(sizeof(float) * npartials);
   pl.off_norms = lay.take(sizeof(float) * nm);
   pl.off_inv = lay.take(sizeof(float) * nm);
-  // Every matrix small enough for the fused kernel: one launch runs the whole iteration
-  // (DMUON_SMALL_FUSED=0 keeps the phase-by-phase grouped launches instead).
+  // Every matrix small enough for the fused kernel: one launch runs the whole iteration.
   {
-    const char* env = getenv("DMUON_SMALL_FUSED");
-    bool all_small = key.kind != kPlanMomNorm && key.kind != kPlanNsTp && !(env && strcmp(env, "0") == 0);
+    bool all_small = key.kind != kPlanMomNorm && key.kind != kPlanNsTp;
     for (int i = 0; i < nm && all_small; ++i)
       all_small = pl.mats[i].m <= kSmallMaxM && pl.mats[i].n <= kSmallMaxN;
     pl.small_fused = all_small;
@@ -1048,7 +1047,7 @@ int muon_key(int count, float* const* params, const void* const* grads, int grad
   if (grad_dtype != DMUON_F32 && grad_dtype != DMUON_BF16)
     return fail(DMUON_ERR_INVALID_ARG, "grad_dtype must be DMUON_F32 (0) or DMUON_BF16 (1)");
   if (!std::isfinite(lr) || !std::isfinite(beta)) return fail(DMUON_ERR_INVALID_ARG, "lr and beta must be finite");
-  if (norms_out && !aligned16(norms_out) && (reinterpret_cast<uintptr_t>(norms_out) & 3))
+  if (norms_out && (reinterpret_cast<uintptr_t>(norms_out) & 3))
     return fail(DMUON_ERR_INVALID_ARG, "norms_out must be 4-byte aligned");
   st = check_ns_args(coeffs, steps, restarts, n_restarts, backend, eps);
   if (st != DMUON_OK) return st;

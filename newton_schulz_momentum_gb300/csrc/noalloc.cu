@@ -9,10 +9,13 @@
 //
 // The array's name in host code is only a host-side stand-in, never a device address: the first call
 // on each device (with that device current) asks the runtime for the real address with
-// cudaGetSymbolAddress and keeps it. All calls share the one array, so calls whose work overlaps on the
-// GPU (different streams, or different host threads on one stream without ordering) race on it.
-// Nothing in it needs to start at zero: every call rewrites the descriptor, every partial sum it reads
-// and the norm before using them.
+// cudaGetSymbolAddress and keeps it, together with the unique id of the CUDA context it was found in.
+// When a later call finds another context current on that device (after cudaDeviceReset, for instance,
+// the runtime loads the library's device image into a new primary context, where the array may sit
+// elsewhere) the address is looked up again. All calls share the one array, so calls whose work
+// overlaps on the GPU (different streams, or different host threads on one stream without ordering)
+// race on it. Nothing in it needs to start at zero: every call rewrites the descriptor, every partial
+// sum it reads and the norm before using them.
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -49,15 +52,47 @@ __global__ void noalloc_describe_kernel(NoAllocScratch* s, RowMat mat, int64_t n
 constexpr int kMaxDevices = 64;
 std::mutex g_noalloc_mu;
 NoAllocScratch* g_noalloc_addr[kMaxDevices] = {};
+unsigned long long g_noalloc_ctx[kMaxDevices] = {};
 
-// Device address of the scratch on the current device (looked up once per device).
+// Unique id of the calling thread's current CUDA context (cuCtxGetCurrent + cuCtxGetId from the driver
+// entry points); 0 when no context is current or the driver cannot say.
+unsigned long long current_context_id() {
+  typedef CUresult (*GetCurrentFn)(CUcontext*);
+  typedef CUresult (*GetIdFn)(CUcontext, unsigned long long*);
+  static GetCurrentFn get_current = nullptr;
+  static GetIdFn get_id = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* a = nullptr;
+    void* b = nullptr;
+    cudaDriverEntryPointQueryResult qa, qb;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &a, 12000, cudaEnableDefault, &qa) == cudaSuccess &&
+        qa == cudaDriverEntryPointSuccess &&
+        cudaGetDriverEntryPointByVersion("cuCtxGetId", &b, 12000, cudaEnableDefault, &qb) == cudaSuccess &&
+        qb == cudaDriverEntryPointSuccess) {
+      get_current = reinterpret_cast<GetCurrentFn>(a);
+      get_id = reinterpret_cast<GetIdFn>(b);
+    } else {
+      cudaGetLastError();
+    }
+  }
+  if (!get_current || !get_id) return 0;
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr || get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+// Device address of the scratch on the current device: looked up once per device and context.
 int scratch_address(NoAllocScratch** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return set_error(DMUON_ERR_CUDA, "cudaGetDevice failed");
   if (dev < 0 || dev >= kMaxDevices) return set_error(DMUON_ERR_UNSUPPORTED, "device ordinal out of range");
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (!g_noalloc_addr[dev]) {
+  const unsigned long long ctx = current_context_id();
+  if (!g_noalloc_addr[dev] || ctx == 0 || ctx != g_noalloc_ctx[dev]) {
     int major = 0, minor = 0;
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
@@ -68,6 +103,7 @@ int scratch_address(NoAllocScratch** out) {
     if (e != cudaSuccess || ptr == nullptr)
       return set_error(DMUON_ERR_CUDA, "cudaGetSymbolAddress of the no-alloc scratch failed");
     g_noalloc_addr[dev] = static_cast<NoAllocScratch*>(ptr);
+    g_noalloc_ctx[dev] = current_context_id();  // the lookup made the device's primary context current
   }
   *out = g_noalloc_addr[dev];
   return DMUON_OK;

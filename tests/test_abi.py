@@ -213,3 +213,30 @@ def test_header_serves_a_plain_c_client(L, tmp_path):
     assert [int(v) for v in out[:3]] == list(owners)
     assert [float(v) for v in out[3:5]] == list(loads)
     assert int(out[5]) == dm.workspace_size(shapes, "gram")
+
+
+def test_noalloc_arguments_rejected_without_device(L):
+    """dmuon_momentum_normalize_noalloc checks every argument before it looks up its scratch or touches a
+    device: NULL buffers, misaligned buffers, a bad gradient type, empty or oversized shapes, non-finite
+    beta or eps."""
+    f = L.dmuon_momentum_normalize_noalloc
+    A, B, C = 4096, 8192, 12288  # 16-byte aligned stand-in addresses (never dereferenced)
+    cases = [
+        ((None, 0, None, 4, 8, B, C, 0.95, 1e-7), "NULL"),
+        ((None, 0, A, 4, 8, None, C, 0.95, 1e-7), "NULL"),
+        ((None, 0, A, 4, 8, B, None, 0.95, 1e-7), "NULL"),
+        ((None, 2, A, 4, 8, B, C, 0.95, 1e-7), "grad_dtype"),
+        ((None, 0, A + 4, 4, 8, B, C, 0.95, 1e-7), "aligned"),
+        ((None, 0, A, 4, 8, B + 8, C, 0.95, 1e-7), "aligned"),
+        ((A + 8, 1, A, 4, 8, B, C, 0.95, 1e-7), "aligned"),
+        ((None, 0, A, 4, 8, B, C + 2, 0.95, 1e-7), "aligned"),
+        ((None, 0, A, 0, 8, B, C, 0.95, 1e-7), "rows and cols"),
+        ((None, 0, A, 4, -1, B, C, 0.95, 1e-7), "rows and cols"),
+        ((None, 0, A, 1 << 20, 1 << 9, B, C, 0.95, 1e-7), "DMUON_NOALLOC_MAX_ELEMS"),
+        ((None, 0, A, 4, 8, B, C, float("nan"), 1e-7), "beta"),
+        ((None, 0, A, 4, 8, B, C, 0.95, float("inf")), "eps"),
+        ((None, 0, A, 4, 8, B, C, 0.95, -1e-7), "eps"),
+    ]
+    for args, word in cases:
+        rc, msg = _status(L, f(*args, None))
+        assert rc == dm.ERR_INVALID_ARG and word in msg, (args, msg)

@@ -46,12 +46,56 @@ def test_stale_digest_hides_the_capture(tmp_path, monkeypatch):
 
 
 def test_total_flops_counts_every_matrix():
+    """value counts Gram as 6 m^2 n + 20 m^3 (S = (aI+Z) R a full product); as_executed as the library
+    computes it, 6 m^2 n + 17 m^3; direct 15 m^2 n + 5 m^3 either way."""
     import newton_schulz_momentum_gb300 as dm
     shapes = [("a", 128, 512), ("b", 512, 128), ("c", 4096, 4096)]
-    assert bench.total_flops(shapes, "gram") == sum(dm.gram_flops(r, c) for _, r, c in shapes)
+
+    def alg(r, c):
+        m, n = min(r, c), max(r, c)
+        return 6 * m * m * n + 20 * m ** 3
+
+    assert bench.total_flops(shapes, "gram") == sum(alg(r, c) for _, r, c in shapes)
+    assert bench.total_flops(shapes, "gram", as_executed=True) == sum(dm.gram_flops(r, c) for _, r, c in shapes)
     assert bench.total_flops(shapes, "direct") == sum(dm.direct_flops(r, c) for _, r, c in shapes)
     auto = bench.total_flops(shapes, "auto")
-    assert auto == dm.gram_flops(128, 512) + dm.gram_flops(512, 128) + dm.direct_flops(4096, 4096)
+    assert auto == alg(128, 512) + alg(512, 128) + dm.direct_flops(4096, 4096)
+
+
+def test_headline_flop_total_matches_the_closed_form():
+    """The whole Llama-3-8B set: 387.85 TFLOP per Gram step on the algorithmic count, 354.66 as executed."""
+    import workloads
+    shapes = workloads.llama3_8b_shapes(32)
+    assert round(bench.total_flops(shapes, "gram") / 1e12, 2) == 387.85
+    assert round(bench.total_flops(shapes, "gram", as_executed=True) / 1e12, 2) == 354.66
+
+
+def test_owned_shapes_partition_the_set():
+    """--owned: every matrix belongs to exactly one rank's share, and each share is what
+    dmuon_assign_owners gives that rank."""
+    import workloads
+    shapes = workloads.llama3_8b_shapes(32)
+    for world in (1, 2, 3, 8):
+        shares = [bench.owned_shapes(shapes, world, r) for r in range(world)]
+        names = sorted(n for share in shares for n, _, _ in share)
+        assert names == sorted(n for n, _, _ in shapes)
+
+
+def test_reference_extrapolation_covers_every_shape():
+    """The reference arm's distinct oriented shapes and their counts add up to the workload."""
+    import workloads
+    shapes = workloads.llama3_8b_shapes(32)
+    distinct = bench.distinct_oriented(shapes)
+    assert sorted((min(r, c), max(r, c)) for r, c, _ in distinct) == [(1024, 4096), (4096, 4096), (4096, 14336)]
+    assert sum(n for _, _, n in distinct) == 224
+    small = [(f"m{i}", r, c) for i, (r, c) in enumerate(workloads.small_set_shapes())]
+    assert [(min(r, c), max(r, c), n) for r, c, n in bench.distinct_oriented(small)] == [(128, 512, 2560)]
+
+
+def test_cpu_info_names_the_host():
+    info = bench.cpu_info()
+    assert set(info) == {"cpu_model", "blas", "numpy"}
+    assert info["numpy"]
 
 
 def test_peaks_read_the_measured_file_or_fall_back():

@@ -44,3 +44,37 @@ def test_bounded_wait_times_out_and_reports(dm):
     want = a.astype(np.float64) @ a.astype(np.float64).T
     got = d.float().cpu().numpy()
     assert np.linalg.norm(got - want) <= 2e-3 * np.linalg.norm(want)
+
+
+def test_workspace_limit_reports_oom_before_any_launch(dm):
+    """A call whose plan needs more workspace than the set limit fails with DMUON_ERR_OOM and a message
+    naming the limit, before anything is launched: no kernel ran (the per-launch record stays empty), and
+    W and M are untouched. The same call goes through once the limit is lifted."""
+    import workloads
+
+    shapes = [(300, 1000), (1000, 300), (256, 1024)]
+    W0 = [workloads.gaussian(s, 0.02, 40 + i) for i, s in enumerate(shapes)]
+    M0 = [workloads.gaussian(s, 1e-3, 50 + i) for i, s in enumerate(shapes)]
+    G = [torch.from_numpy(workloads.gaussian(s, 1e-3, 60 + i)).cuda() for i, s in enumerate(shapes)]
+    W = [torch.from_numpy(w).cuda() for w in W0]
+    M = [torch.from_numpy(m).cuda() for m in M0]
+    need = dm.workspace_size(shapes, "gram")
+    dm.release_workspace()  # the call below must plan and bind anew
+    dm.set_workspace_limit(need // 2)
+    dm.timing_enable(True)
+    try:
+        with pytest.raises(dm.DmuonError) as ei:
+            dm.muon_step(W, G, M, lr=0.02, beta=0.95, coeffs=dm.YOU, restarts=(2,), backend="gram")
+        assert ei.value.status == dm.ERR_OOM
+        assert "exceeds the limit" in str(ei.value)
+        assert dm.timing_read_launches() == []
+    finally:
+        dm.timing_enable(False)
+        dm.set_workspace_limit(0)
+    torch.cuda.synchronize()
+    for w, w0, m, m0 in zip(W, W0, M, M0):
+        assert np.array_equal(w.cpu().numpy(), w0)
+        assert np.array_equal(m.cpu().numpy(), m0)
+    dm.muon_step(W, G, M, lr=0.02, beta=0.95, coeffs=dm.YOU, restarts=(2,), backend="gram")
+    dm.check_status()
+    assert not np.array_equal(W[0].cpu().numpy(), W0[0])

@@ -322,8 +322,13 @@ def test_small_fused_ns_in_place(dm):
 
 def test_small_matrix_set_one_grouped_step(dm):
     """2048 gradients of 128 x 512 plus 512 of 512 x 128, N(0, 1e-3^2), beta 0.95 from zero, Gram with
-    restart [2]: the whole iteration of all 2560 matrices in one fused launch. Graded with YOU; the printed POLAR_EXPRESS set is run too
-    and checked only for finiteness and a looser bound (its fp16 error on this shape sits near 3e-2)."""
+    restart [2]: the whole iteration of all 2560 matrices in one fused launch. Graded with YOU at 2e-2. The
+    printed POLAR_EXPRESS set is run too and held to 6e-2: on these Gaussian 128 x 512 matrices the
+    normalised singular values lie in [0.044, 0.133], where the composition of the printed POLAR_EXPRESS
+    polynomials runs from 1.02 up to 2.5e5 with slopes up to 4e7, so fp16 rounding of the intermediates is
+    amplified far more than with YOU (range 0.98 .. 1.03, slopes below 12). Any fp16 iteration lands near
+    5e-2 here: a NumPy emulation of the same fp16-operand, fp32-accumulation Gram iteration gives 5.2e-2
+    on this shape, and the kernel measures 4.9e-2."""
     shapes = workloads.small_set_shapes()
     G = [workloads.gaussian(s, 1e-3, 1000 + i) for i, s in enumerate(shapes)]
     W = [workloads.gaussian(s, 0.02, 5000 + i) for i, s in enumerate(shapes)]
@@ -341,32 +346,54 @@ def test_small_matrix_set_one_grouped_step(dm):
             assert check_update(W[i], Wd[i].cpu().numpy(), ref, 0.02) <= tol
 
 
-def _llama_run(dm, layers, seed, sample_names, backend, check_direct_too=False):
-    """Muon step over `layers` Llama-3-8B layers of Muon-target matrices, bf16 grads N(0, 1e-3^2), fp32 W
-    N(0, 0.02^2), zero momentum, POLAR_EXPRESS, Gram restart [2]. The sampled matrices get host-generated
-    inputs (seeded per matrix); the others are filled on the device and are not compared."""
+def _llama_run(dm, layers, seed, sample_names, backend):
+    """Two Muon steps over `layers` Llama-3-8B layers of Muon-target matrices: bf16 grads N(0, 1e-3^2), fp32 W
+    N(0, 0.02^2), POLAR_EXPRESS, Gram restart [2]. Step 1 starts from zero momentum; step 2 takes a second
+    seeded gradient on top of step 1's momentum, so M <- beta M + G runs with M != 0 through the bulk-copy
+    momentum pass at full size. The sampled matrices get host-generated gradients and weights (seeded per
+    matrix and step) and are compared with the oracle after each step on M and ||M|| (1e-5) and on the
+    update (W_before - W_after) / lr (2e-2), the oracle taking the GPU's W and M from before the step; the
+    other matrices are filled on the device and are not compared. The device buffers stay the same across
+    the two steps (new gradients are copied into them), as in a training loop."""
     shapes = workloads.llama3_8b_shapes(layers)
     gen = torch.Generator(device="cuda")
     gen.manual_seed(seed)
     Wd, Gd, Md, host = [], [], [], {}
     for i, (name, r, c) in enumerate(shapes):
         if name in sample_names:
-            g, bits = workloads.round_to_bf16(workloads.gaussian((r, c), 1e-3, seed * 1000 + i))
+            grads = [workloads.round_to_bf16(workloads.gaussian((r, c), 1e-3, seed * 1000 + 250 * s + i))
+                     for s in (0, 2)]
             w = workloads.gaussian((r, c), 0.02, seed * 1000 + 500 + i)
-            host[i] = (w, g)
-            Gd.append(torch.from_numpy(bits.view(np.int16)).cuda().view(torch.bfloat16))
+            host[i] = grads
+            Gd.append(torch.empty((r, c), dtype=torch.bfloat16, device="cuda"))
             Wd.append(cuda(w))
         else:
-            Gd.append((torch.randn((r, c), generator=gen, device="cuda") * 1e-3).to(torch.bfloat16))
+            Gd.append(torch.empty((r, c), dtype=torch.bfloat16, device="cuda"))
             Wd.append(torch.randn((r, c), generator=gen, device="cuda") * 0.02)
         Md.append(torch.zeros((r, c), dtype=torch.float32, device="cuda"))
-    dm.muon_step(Wd, Gd, Md, lr=0.02, beta=0.95, coeffs=dm.POLAR_EXPRESS, restarts=(2,), backend=backend)
-    dm.check_status()
-    for i, (w, g) in host.items():
-        ref = muon_ref(w, g, np.zeros_like(w), 0.02, 0.95, ns64.POLAR_EXPRESS, (2,), backend)
-        assert rel(Md[i].cpu().numpy(), ref["M"]) <= TOL_F32, shapes[i][0]
-        err = check_update(w, Wd[i].cpu().numpy(), ref, 0.02)
-        assert err <= TOL_NS, (shapes[i][0], err)
+    norms = torch.empty(len(shapes), dtype=torch.float32, device="cuda")
+    for step in range(2):
+        for i, (name, r, c) in enumerate(shapes):
+            if i in host:
+                bits = host[i][step][1]
+                Gd[i].copy_(torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16))
+            else:
+                Gd[i].copy_((torch.randn((r, c), generator=gen, device="cuda") * 1e-3).to(torch.bfloat16))
+        before = {i: (Wd[i].cpu().numpy().astype(np.float64), Md[i].cpu().numpy().astype(np.float64)) for i in host}
+        dm.muon_step(Wd, Gd, Md, lr=0.02, beta=0.95, coeffs=dm.POLAR_EXPRESS, restarts=(2,), backend=backend,
+                     norms_out=norms)
+        dm.check_status()
+        nh = norms.cpu().numpy()
+        for i, (w0, m0) in before.items():
+            if step == 0:
+                assert not np.any(m0)
+            g = host[i][step][0]
+            ref = muon_ref(w0, g, m0, 0.02, 0.95, ns64.POLAR_EXPRESS, (2,), backend)
+            where = (shapes[i][0], f"step {step + 1}")
+            assert rel(Md[i].cpu().numpy(), ref["M"]) <= TOL_F32, where
+            assert abs(nh[i] - ref["norm"]) <= TOL_F32 * ref["norm"], where
+            err = check_update(w0, Wd[i].cpu().numpy(), ref, 0.02)
+            assert err <= TOL_NS, (where, err)
     del Wd, Gd, Md
     torch.cuda.empty_cache()
 
