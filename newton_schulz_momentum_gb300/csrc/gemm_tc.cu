@@ -48,13 +48,17 @@ struct Cfg {
   static constexpr int kABytes = kBM * kBK * 2;  // 16 KB
   static constexpr int kBBytes = kBRows * kBK * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
-  static constexpr int kStages = (kStageBytes <= 32768) ? 6 : 4;
-  static constexpr int kTmemCols = 2 * BN;  // two accumulators of BN fp32 columns
   // Epilogue warps: one per TMEM lane quarter, or two (each draining half of the tile's columns) for the
-  // 128 x 128 tiles of launches too small to fill the machine, whose epilogue is their critical path.
-  static constexpr int kEpiWarps = (BN == 128 && CG == 1) ? 8 : 4;
+  // 128 x 128 tiles of launches too small to fill the machine, whose epilogue is their critical path;
+  // those also double-buffer their staging (a chunk is written while the previous one's stores read the
+  // other buffer) and keep five ring stages to make room.
+  static constexpr bool kSmallTile = BN == 128 && CG == 1;
+  static constexpr int kStages = kSmallTile ? 5 : (kStageBytes <= 32768) ? 6 : 4;
+  static constexpr int kTmemCols = 2 * BN;  // two accumulators of BN fp32 columns
+  static constexpr int kEpiWarps = kSmallTile ? 8 : 4;
+  static constexpr int kEpiBufs = kSmallTile ? 2 : 1;  // 4 KB staging buffers per epilogue warp
   static constexpr int kThreads = 64 + 32 * kEpiWarps;
-  static constexpr int kEpiBytes = kEpiWarps * 4096;  // one 4 KB staging buffer per epilogue warp
+  static constexpr int kEpiBytes = kEpiWarps * 4096 * kEpiBufs;
   static constexpr int kBarrierBytes = 256;
   static constexpr int kSmemBytes = kStages * kStageBytes + kEpiBytes + kBarrierBytes + 1024;  // + alignment slack
   static_assert(kStageBytes % 1024 == 0, "stages must keep 1024-byte alignment for 128B swizzle");
@@ -133,11 +137,31 @@ __device__ __forceinline__ void reduce_out(const CUtensorMap* map, uint32_t src,
   else tma_reduce_add_2d(map, src, c0, c1);
 }
 
-// One warp's share of a tile: the 32 rows of TMEM lane quarter `quarter`, columns [c_lo, c_hi) of the tile.
+// The addend of this warp's first chunk of a tile (zeros when there is none). It was written by an earlier
+// launch, so it is loaded before the tile's products complete and its latency hides behind them.
 template <int BN>
+__device__ __forceinline__ void load_first_e(const GemmLaunch& p, const GemmJob& job, int tile_row0, int tn,
+                                             int quarter, int c_lo, int c_hi, int lane, uint4 (&e)[4]) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) e[q] = make_uint4(0, 0, 0, 0);
+  const int row0 = tile_row0 + quarter * 32;
+  const int i = row0 + lane;
+  if (row0 >= job.M || i >= job.M || job.E == nullptr || recipe_scalars(p, job.recipe).e == 0.f) return;
+  const int c = (job.flags & kJobSymmetric) ? max(c_lo, row0 - tn * BN) : c_lo;
+  if (c < c_hi && tn * BN + c + 32 <= job.N) {
+    const uint4* e4 = reinterpret_cast<const uint4*>(job.E + static_cast<int64_t>(i) * job.lde + tn * BN + c);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) e[q] = e4[q];
+  }
+}
+
+// One warp's share of a tile: the 32 rows of TMEM lane quarter `quarter`, columns [c_lo, c_hi) of the tile.
+// `ecur` holds the first chunk's addend (load_first_e). With kBufs = 2 the warp's staging is two 4 KB
+// buffers used in turn (`chunk` counts this warp's chunks across tiles), otherwise one.
+template <int BN, int kBufs>
 __device__ void epilogue_tile(const GemmLaunch& p, const GemmJob& job, int tile_row0, int tn, int quarter,
-                              int c_lo, int c_hi, int lane, uint32_t taddr, uint8_t* stage, bool& bad,
-                              uint64_t pol_out) {
+                              int c_lo, int c_hi, int lane, uint32_t taddr, uint8_t* stage_base, int& chunk,
+                              uint4 (&ecur)[4], bool& bad, uint64_t pol_out) {
   const int row0 = tile_row0 + quarter * 32;  // first row handled by this warp
   if (row0 >= job.M) return;                  // all 32 rows past the edge: nothing to read or store
   const int i = row0 + lane;
@@ -150,7 +174,6 @@ __device__ void epilogue_tile(const GemmLaunch& p, const GemmJob& job, int tile_
   const bool row_ok = i < job.M;
   const __half* erow = (job.E != nullptr && s.e != 0.f && row_ok) ? job.E + static_cast<int64_t>(i) * job.lde : nullptr;
   const bool has_e = job.E != nullptr && s.e != 0.f;
-  const uint32_t sbuf = smem_u32(stage);
   const bool scale = s.acc != 1.f;
   // Overflow / NaN detection without per-element compares: an fp16 (or, for the final output, fp32)
   // value that is inf or NaN times zero is NaN, so one packed FMA per pair of outputs folds the check into
@@ -163,18 +186,16 @@ __device__ void epilogue_tile(const GemmLaunch& p, const GemmJob& job, int tile_
   // Symmetric outputs: chunks left of the diagonal block are produced by the mirrored stores of other
   // tiles, so this warp starts at its diagonal block (row0 and tn*BN are multiples of 32).
   int c = sym ? max(c_lo, row0 - tn * BN) : c_lo;
-  uint4 ecur[4], enext[4];
+  uint4 enext[4];
 #pragma unroll
-  for (int q = 0; q < 4; ++q) ecur[q] = make_uint4(0, 0, 0, 0), enext[q] = ecur[q];
-  if (erow && c < c_hi && tn * BN + c + 32 <= job.N) {
-    const uint4* e4 = reinterpret_cast<const uint4*>(erow + tn * BN + c);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) ecur[q] = e4[q];
-  }
+  for (int q = 0; q < 4; ++q) enext[q] = make_uint4(0, 0, 0, 0);
 
   for (; c < c_hi; c += 32) {
     const int j0 = tn * BN + c;
     if (j0 >= job.N) break;  // warp-uniform
+    uint8_t* const stage = stage_base + (kBufs > 1 ? (chunk & 1) * 4096 : 0);
+    const uint32_t sbuf = smem_u32(stage);
+    ++chunk;
     const bool full = j0 + 32 <= job.N;
     const bool prefetch = erow != nullptr && c + 32 < c_hi && j0 + 64 <= job.N;
     if (prefetch) {
@@ -225,7 +246,7 @@ __device__ void epilogue_tile(const GemmLaunch& p, const GemmJob& job, int tile_
 #pragma unroll
       for (int k = 0; k < 32; ++k) chk32 = fmaf(v[k], 0.f, chk32);
       if (tma_w) {
-        if (lane == 0) bulk_wait_read0();
+        if (lane == 0) bulk_wait_read_allow<kBufs - 1>();  // this buffer's previous stores have read it
         __syncwarp();
         if (!final_trans) {
 #pragma unroll
@@ -274,7 +295,7 @@ __device__ void epilogue_tile(const GemmLaunch& p, const GemmJob& job, int tile_
     const bool upper = sym && j0 > row0;  // strictly above the diagonal for every row of the block
     const bool on_diag = j0 == row0;      // the block holds the diagonal elements i == j
 
-    if (lane == 0) bulk_wait_read0();  // the previous chunk's stores have read the buffer
+    if (lane == 0) bulk_wait_read_allow<kBufs - 1>();  // this buffer's previous stores have read it
     __syncwarp();
 #pragma unroll
     for (int q = 0; q < 4; ++q)
@@ -537,17 +558,21 @@ __device__ __forceinline__ void gemm_tc_body(const GemmLaunch& p) {
     int acc = 0;
     uint32_t acc_phase = 0;
     bool bad = false;
+    int chunk = 0;  // this warp's chunks so far (which staging buffer is next)
     for (int t = unit; t < p.ntiles; t += nunits) {
       const TileRef tr = tile_at(p, t, BN, C::kTileM);
       if (tr.skip) continue;
+      const int tile_row0 = tr.tm * C::kTileM + static_cast<int>(rank) * kBM;
+      uint4 efirst[4];
+      load_first_e<BN>(p, *tr.job, tile_row0, tr.tn, quarter, c_lo, c_lo + kSpan, lane, efirst);
       bool ok = wait_bounded(&tfull[acc], acc_phase, abort_flag, p.status, kWaitLimitNs, true);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
       const uint32_t taddr =
           tmem_base + static_cast<uint32_t>(acc * BN) + (static_cast<uint32_t>(quarter * 32) << 16);
-      epilogue_tile<BN>(p, *tr.job, tr.tm * C::kTileM + static_cast<int>(rank) * kBM, tr.tn, quarter, c_lo,
-                        c_lo + kSpan, lane, taddr, epi_stage + (warp - 2) * 4096, bad, pol_out);
+      epilogue_tile<BN, C::kEpiBufs>(p, *tr.job, tile_row0, tr.tn, quarter, c_lo, c_lo + kSpan, lane, taddr,
+                                     epi_stage + (warp - 2) * 4096 * C::kEpiBufs, chunk, efirst, bad, pol_out);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {

@@ -347,6 +347,11 @@ __device__ __forceinline__ void bulk_load_hint(uint32_t smem_dst, const void* sr
 
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// Wait until at most N of this thread's most recent bulk groups are still reading shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read_allow() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
 __device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // Byte offset of element (r, c) of a 32 x 32 fp16 block: 64-byte rows, 16-byte units swizzled by the
