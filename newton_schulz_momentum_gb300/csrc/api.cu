@@ -317,11 +317,19 @@ JobSpec make_job(int mat, int M, int N, int K, int recipe, int flags, size_t a, 
 constexpr bool kMirrorS = true;
 constexpr bool kMirrorQ = false;
 
+// A matrix with m <= kFullSymMaxM computes its symmetric products (X X^T, R^2, the R update) in full
+// instead of as upper triangle + mirror: at most 2 x 2 output tiles, so the extra tile runs beside the
+// others, while a mirrored chunk costs its warp about three times a plain one (the transposed staging
+// and the second store) on the phase's critical path. The choice depends on the matrix alone, so a
+// matrix gets the same arithmetic whatever else is in the call.
+constexpr int64_t kFullSymMaxM = 256;
+int sym_flag(const MatInfo& mi) { return mi.m <= kFullSymMaxM ? 0 : kJobSymmetric; }
+
 void build_gram_phases(Plan& pl, const std::vector<int>& restarts, int steps, const std::vector<int>& idx,
                        std::vector<std::vector<JobSpec>>& out, std::vector<int>& out_coef) {
   const int nm = static_cast<int>(pl.mats.size());
-  const int s_flag = kMirrorS ? kJobSymmetric : 0;
-  const int q_flag = kMirrorQ ? kJobSymmetric : 0;
+  const int s_mirror = kMirrorS ? kJobSymmetric : 0;
+  const int q_mirror = kMirrorQ ? kJobSymmetric : 0;
   std::vector<char> is_restart(steps + 1, 0);
   for (int r : restarts)
     if (r > 0 && r < steps) is_restart[r] = 1;
@@ -362,7 +370,7 @@ void build_gram_phases(Plan& pl, const std::vector<int>& restarts, int steps, co
     std::vector<JobSpec> ph;
     for (int i : idx) {
       const MatInfo& mi = pl.mats[i];
-      ph.push_back(make_job(i, mi.m, mi.m, mi.n, kRecPlain, kJobSymmetric, X[i], mi.ldx, X[i], mi.ldx, kNone, 0,
+      ph.push_back(make_job(i, mi.m, mi.m, mi.n, kRecPlain, sym_flag(mi), X[i], mi.ldx, X[i], mi.ldx, kNone, 0,
                             mi.R, mi.ldm));
     }
     push(std::move(ph), coef);
@@ -387,7 +395,7 @@ void build_gram_phases(Plan& pl, const std::vector<int>& restarts, int steps, co
       std::vector<JobSpec> ph;
       for (int i : idx) {
         const MatInfo& mi = pl.mats[i];
-        ph.push_back(make_job(i, mi.m, mi.m, mi.m, kRecZ, kJobSymmetric | (fresh ? kJobD2 : 0), mi.R, mi.ldm, mi.R,
+        ph.push_back(make_job(i, mi.m, mi.m, mi.m, kRecZ, sym_flag(mi) | (fresh ? kJobD2 : 0), mi.R, mi.ldm, mi.R,
                               mi.ldm, mi.R, mi.ldm, mi.Z, mi.ldm, fresh ? Q[i] : kNone));
       }
       push(std::move(ph), k);
@@ -398,12 +406,12 @@ void build_gram_phases(Plan& pl, const std::vector<int>& restarts, int steps, co
       for (int i : idx) {
         const MatInfo& mi = pl.mats[i];
         if (!fresh) {  // Q' = Z Q + a Q
-          ph.push_back(make_job(i, mi.m, mi.m, mi.m, kRecAxpy, kJobBMnMajor | q_flag, mi.Z, mi.ldm, Q[i], mi.ldm, Q[i],
-                                mi.ldm, Qb[i], mi.ldm));
+          ph.push_back(make_job(i, mi.m, mi.m, mi.m, kRecAxpy, kJobBMnMajor | (q_mirror & sym_flag(mi)), mi.Z, mi.ldm,
+                                Q[i], mi.ldm, Q[i], mi.ldm, Qb[i], mi.ldm));
         }
         if (update_r) {  // S = Z R + a R
-          ph.push_back(make_job(i, mi.m, mi.m, mi.m, kRecAxpy, s_flag, mi.Z, mi.ldm, mi.R, mi.ldm, mi.R, mi.ldm, mi.S,
-                                mi.ldm));
+          ph.push_back(make_job(i, mi.m, mi.m, mi.m, kRecAxpy, s_mirror & sym_flag(mi), mi.Z, mi.ldm, mi.R, mi.ldm,
+                                mi.R, mi.ldm, mi.S, mi.ldm));
         }
       }
       push(std::move(ph), k);
@@ -414,7 +422,7 @@ void build_gram_phases(Plan& pl, const std::vector<int>& restarts, int steps, co
       std::vector<JobSpec> ph;
       for (int i : idx) {
         const MatInfo& mi = pl.mats[i];
-        ph.push_back(make_job(i, mi.m, mi.m, mi.m, kRecAxpy, kJobSymmetric, mi.S, mi.ldm, mi.Z, mi.ldm, mi.S, mi.ldm,
+        ph.push_back(make_job(i, mi.m, mi.m, mi.m, kRecAxpy, sym_flag(mi), mi.S, mi.ldm, mi.Z, mi.ldm, mi.S, mi.ldm,
                               mi.R, mi.ldm));
       }
       push(std::move(ph), k);
@@ -445,9 +453,9 @@ void build_direct_phases(Plan& pl, int steps, const std::vector<int>& idx, std::
     for (int i : idx) {
       const MatInfo& mi = pl.mats[i];
       // A = X X^T (in R), B = b A + c A^2 (in Z)
-      p1.push_back(make_job(i, mi.m, mi.m, mi.n, kRecPlain, kJobSymmetric, X[i], mi.ldx, X[i], mi.ldx, kNone, 0, mi.R,
+      p1.push_back(make_job(i, mi.m, mi.m, mi.n, kRecPlain, sym_flag(mi), X[i], mi.ldx, X[i], mi.ldx, kNone, 0, mi.R,
                             mi.ldm));
-      p2.push_back(make_job(i, mi.m, mi.m, mi.m, kRecZ, kJobSymmetric, mi.R, mi.ldm, mi.R, mi.ldm, mi.R, mi.ldm, mi.Z,
+      p2.push_back(make_job(i, mi.m, mi.m, mi.m, kRecZ, sym_flag(mi), mi.R, mi.ldm, mi.R, mi.ldm, mi.R, mi.ldm, mi.Z,
                             mi.ldm));
       if (k + 1 < steps) {  // X' = B X + a X
         p3.push_back(make_job(i, mi.m, mi.n, mi.m, kRecAxpy, kJobBMnMajor, mi.Z, mi.ldm, X[i], mi.ldx, X[i], mi.ldx,
