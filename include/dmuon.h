@@ -53,7 +53,8 @@ typedef enum dmuon_status {
   DMUON_ERR_OOM = 3,         /* workspace allocation failed or exceeds the set limit           */
   DMUON_ERR_CUDA = 4,        /* a CUDA runtime/driver call failed (text in dmuon_last_error)  */
   DMUON_ERR_TIMEOUT = 5,     /* a device-side bounded wait gave up (reported by check_status)  */
-  DMUON_ERR_NONFINITE = 6    /* an fp16 intermediate overflowed or became NaN (check_status)   */
+  DMUON_ERR_NONFINITE = 6,   /* an fp16 intermediate overflowed or became NaN (check_status)   */
+  DMUON_ERR_RANGE = 7        /* checked build only: a device-side range check failed (check_status) */
 } dmuon_status;
 
 typedef enum dmuon_ns_backend {
@@ -275,8 +276,9 @@ DMUON_API int dmuon_adamw_step(int count, float* const* params, const void* cons
 /*
  * dmuon_check_status -- synchronise `cuda_stream`, then read and clear the device status word.
  * Returns DMUON_OK, DMUON_ERR_TIMEOUT (a kernel's bounded wait gave up: its results are invalid),
- * DMUON_ERR_NONFINITE (an fp16 intermediate overflowed or was NaN) or DMUON_ERR_CUDA (an
- * asynchronous CUDA error surfaced during synchronisation).
+ * DMUON_ERR_RANGE (checked build: an index or tile outside its table or matrix was found and skipped;
+ * results are invalid), DMUON_ERR_NONFINITE (an fp16 intermediate overflowed or was NaN) or
+ * DMUON_ERR_CUDA (an asynchronous CUDA error surfaced during synchronisation).
  */
 DMUON_API int dmuon_check_status(void* cuda_stream);
 
@@ -320,10 +322,22 @@ DMUON_API int dmuon_plan_info(double* exec_flops_out, int64_t* tiles_out, int* g
  */
 DMUON_API int dmuon_selftest_bounded_wait(int64_t limit_ns, void* cuda_stream);
 
+/*
+ * The checked build. libdmuon_checked.so is built from the same sources with device-side range checks
+ * compiled in (the debugging stand-in for a memory checker): every tile's job index and position, every
+ * row-wise chunk's matrix, partial-sum slot and cast tile, every AdamW chunk and every small-matrix job's
+ * sizes are tested before use; a failed test skips the access and records DMUON_ERR_RANGE for
+ * dmuon_check_status. The regular libdmuon.so leaves them out. dmuon_selftest_range_check launches one
+ * GEMM whose only tile lies outside its (empty) product, so that in the checked build the next
+ * dmuon_check_status returns DMUON_ERR_RANGE; nothing is read or written. In the regular build it returns
+ * DMUON_ERR_UNSUPPORTED without launching. No counterpart on the pages.
+ */
+DMUON_API int dmuon_selftest_range_check(void* cuda_stream);
+
 /* Text of the last error on the calling thread; valid until the next call on that thread. */
 DMUON_API const char* dmuon_last_error(void);
 
-/* Library version string, e.g. "dmuon-gb300 0.1.0 (sm_103a)". */
+/* Library version string, e.g. "dmuon-gb300 0.2.0 (sm_103a)"; the checked build says so. */
 DMUON_API const char* dmuon_version(void);
 
 /* Upper bound on workspace bytes per device (0 = no limit). Calls needing more fail with

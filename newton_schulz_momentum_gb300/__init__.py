@@ -19,7 +19,10 @@ import os
 from typing import Sequence
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libdmuon.so")
+# DMUON_LIBRARY=checked loads the build with device-side range checks (libdmuon_checked.so) instead.
+LIB_PATH = os.path.join(_HERE, "libdmuon_checked.so" if os.environ.get("DMUON_LIBRARY") == "checked"
+                        else "libdmuon.so")
+CHECKED_LIB_PATH = os.path.join(_HERE, "libdmuon_checked.so")
 
 # Coefficient tables printed on the DMuon "Newton-Schulz 变体" page, section "系数集".
 POLAR_EXPRESS = (
@@ -38,8 +41,8 @@ YOU = (
 )
 DEFAULT_RESTARTS = (2,)
 
-OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_OOM, ERR_CUDA, ERR_TIMEOUT, ERR_NONFINITE = range(7)
-_STATUS_NAMES = {1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "OOM", 4: "CUDA", 5: "TIMEOUT", 6: "NONFINITE"}
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_OOM, ERR_CUDA, ERR_TIMEOUT, ERR_NONFINITE, ERR_RANGE = range(8)
+_STATUS_NAMES = {1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "OOM", 4: "CUDA", 5: "TIMEOUT", 6: "NONFINITE", 7: "RANGE"}
 BACKENDS = {"direct": 0, "gram": 1, "auto": 2}
 F32, BF16 = 0, 1
 
@@ -48,7 +51,7 @@ EXPORTS = (
     "dmuon_last_error", "dmuon_version", "dmuon_set_workspace_limit", "dmuon_workspace_size",
     "dmuon_release_workspace", "dmuon_timing_enable", "dmuon_timing_read", "dmuon_momentum_normalize_noalloc",
     "dmuon_assign_owners", "dmuon_adamw_step", "dmuon_ns_tp", "dmuon_muon_step_host",
-    "dmuon_timing_read_launches", "dmuon_plan_info", "dmuon_selftest_bounded_wait",
+    "dmuon_timing_read_launches", "dmuon_plan_info", "dmuon_selftest_bounded_wait", "dmuon_selftest_range_check",
 )
 COST_MODELS = {"elements": 0, "gram_flops": 1, "direct_flops": 2}
 NOALLOC_MAX_ELEMS = 268435456
@@ -104,6 +107,7 @@ def lib():
     L.dmuon_timing_read_launches.argtypes = [i32, ctypes.POINTER(ctypes.c_double), _c_ip, _c_ip]
     L.dmuon_plan_info.argtypes = [ctypes.POINTER(ctypes.c_double), _c_i64p, _c_ip]
     L.dmuon_selftest_bounded_wait.argtypes = [i64, vp]
+    L.dmuon_selftest_range_check.argtypes = [vp]
     for name in EXPORTS:
         if name not in ("dmuon_last_error", "dmuon_version"):
             getattr(L, name).restype = ctypes.c_int
@@ -391,6 +395,12 @@ def selftest_bounded_wait(seconds=0.05, stream=None):
     """Launch one bounded wait that cannot complete (limit `seconds`): the next check_status() raises
     DmuonError with status ERR_TIMEOUT, exactly as when one of the library's waits runs out."""
     _check(lib().dmuon_selftest_bounded_wait(int(seconds * 1e9), _stream(stream)))
+
+
+def selftest_range_check(stream=None):
+    """Checked build only: launch one GEMM whose only tile lies outside its product; the next
+    check_status() raises DmuonError with status ERR_RANGE. The regular build raises ERR_UNSUPPORTED."""
+    _check(lib().dmuon_selftest_range_check(_stream(stream)))
 
 
 def plan_info():

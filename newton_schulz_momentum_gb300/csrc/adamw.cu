@@ -36,8 +36,10 @@ __device__ __forceinline__ void adam_update(float& p, float& m, float& v, float 
 __global__ void __launch_bounds__(kThreads) adamw_kernel(const AdamLaunch a) {
   const int64_t chunk = blockIdx.x;
   const int ti = find_tensor(a.chunk_prefix, a.ntensors, chunk);
+  if (!dev_check(ti >= 0 && ti < a.ntensors, a.status)) return;
   const AdamTensor t = a.tensors[ti];
   const int64_t begin = (chunk - a.chunk_prefix[ti]) * kAdamChunkElems;
+  if (!dev_check(begin >= 0 && begin < t.numel, a.status)) return;
   const int64_t end = min(begin + static_cast<int64_t>(kAdamChunkElems), t.numel);
   const AdamScalars s{a.decay, a.step_size, a.inv_bc2, a.beta1, a.one_minus_beta1, a.beta2, a.one_minus_beta2, a.eps};
   int64_t scalar_from = begin;

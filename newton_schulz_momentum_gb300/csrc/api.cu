@@ -126,7 +126,7 @@ struct Plan {
   // Newton-Schulz phases before the next group starts. One group unless a host-gradient call pipelines
   // its copies against the computation.
   std::vector<int> group_begin;
-  int64_t nchunks = 0, ncast = 0;
+  int64_t nchunks = 0, ncast = 0, npartials = 0;
   size_t off_rowmats = 0, off_chunk = 0, off_tilep = 0, off_partials = 0, off_norms = 0, off_inv = 0;
   size_t off_jobs = 0, off_tiles = 0, bytes = 0;
   // host images uploaded to the arena
@@ -556,6 +556,7 @@ int build_plan_host(Plan& pl, const PlanKey& key, const std::vector<const void*>
     pl.tp_slabs = static_cast<int>((pl.mats[0].m + kShardSlab - 1) / kShardSlab);
     npartials = std::max<int64_t>(npartials, static_cast<int64_t>(key.shards) * pl.tp_slabs);
   }
+  pl.npartials = npartials;
   pl.off_partials = lay.take(sizeof(float) * npartials);
   pl.off_norms = lay.take(sizeof(float) * nm);
   pl.off_inv = lay.take(sizeof(float) * nm);
@@ -820,6 +821,8 @@ int run_plan(DeviceState& ds, const Plan& pl, const float* coeffs, float lr, flo
   rl.beta = beta;
   rl.eps = eps;
   rl.status = ds.status;
+  rl.check_status = ds.status;
+  rl.npartials = pl.npartials;
   const GemmJob* jobs = reinterpret_cast<const GemmJob*>(base + pl.off_jobs);
   const GemmTile* tiles = reinterpret_cast<const GemmTile*>(base + pl.off_tiles);
   const bool overwrite = pl.key.kind == kPlanNs || pl.key.kind == kPlanNsTp;  // W = O, not W -= lr O
@@ -898,6 +901,7 @@ int run_plan(DeviceState& ds, const Plan& pl, const float* coeffs, float lr, flo
       gl.jobs = jobs + L.first_job;
       gl.tiles = tiles + L.first_tile;
       gl.ntiles = L.ntiles;
+      gl.njobs = L.njobs;
       gl.a = coeffs[3 * L.coef + 0];
       gl.b = coeffs[3 * L.coef + 1];
       gl.c = coeffs[3 * L.coef + 2];
@@ -1363,6 +1367,9 @@ int dmuon_check_status(void* cuda_stream) {
   DM_CUDA(cudaMemcpy(&word, ds->status, sizeof(word), cudaMemcpyDeviceToHost), "read device status");
   if (word) DM_CUDA(cudaMemset(ds->status, 0, sizeof(unsigned)), "clear device status");
   if (word & kDevTimeout) return fail(DMUON_ERR_TIMEOUT, "a device-side bounded wait gave up; results are invalid");
+  if (word & kDevRange)
+    return fail(DMUON_ERR_RANGE, "a device-side range check failed (checked build): an index or tile outside its "
+                                 "table or matrix was skipped; results are invalid");
   if (word & kDevNonfinite) return fail(DMUON_ERR_NONFINITE, "an fp16 intermediate overflowed or was NaN");
   return DMUON_OK;
 }
@@ -1451,6 +1458,7 @@ int dmuon_adamw_step(int count, float* const* params, const void* const* grads, 
     a.beta2 = static_cast<float>(beta2);
     a.one_minus_beta2 = static_cast<float>(1.0 - beta2);
     a.eps = static_cast<float>(eps);
+    a.status = ds->status;
     const int64_t nchunks = ap.chunk_prefix[count];
     DM_CUDA(timed(4, stream, [&] { return launch_adamw(a, nchunks, stream); }), "AdamW launch");
     return DMUON_OK;
@@ -1528,6 +1536,30 @@ int dmuon_selftest_bounded_wait(int64_t limit_ns, void* cuda_stream) {
   return DMUON_OK;
 }
 
+int dmuon_selftest_range_check(void* cuda_stream) {
+  if (!DMUON_DEVICE_CHECKS)
+    return fail(DMUON_ERR_UNSUPPORTED, "this library was built without device-side range checks "
+                                       "(libdmuon_checked.so has them)");
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState* ds = nullptr;
+  int st = current_device(&ds);
+  if (st != DMUON_OK) return st;
+  // One GEMM launch whose only tile lies outside its product (a product with no rows): the checks skip it
+  // in every role before any operand is touched and record the failure.
+  GemmLaunch gl;
+  std::memset(&gl, 0, sizeof(gl));
+  gl.single.M = 0;
+  gl.single.N = 128;
+  gl.single.K = 64;
+  gl.single.tiles_n = 1;
+  gl.tiles_m = 1;
+  gl.ntiles = 1;
+  gl.status = ds->status;
+  cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
+  DM_CUDA(launch_gemm(gl, kTileSingle128, 1, stream), "range self-test launch");
+  return DMUON_OK;
+}
+
 int dmuon_plan_info(double* exec_flops_out, int64_t* tiles_out, int* gemm_launches_out) {
   if (!exec_flops_out || !tiles_out || !gemm_launches_out) return fail(DMUON_ERR_INVALID_ARG, "outputs are NULL");
   std::lock_guard<std::mutex> lock(g_mu);
@@ -1546,7 +1578,9 @@ int dmuon_plan_info(double* exec_flops_out, int64_t* tiles_out, int* gemm_launch
 
 const char* dmuon_last_error(void) { return t_last_error.c_str(); }
 
-const char* dmuon_version(void) { return "dmuon-gb300 0.1.0 (sm_103a)"; }
+const char* dmuon_version(void) {
+  return DMUON_DEVICE_CHECKS ? "dmuon-gb300 0.2.0 (sm_103a, device-side range checks)" : "dmuon-gb300 0.2.0 (sm_103a)";
+}
 
 int dmuon_set_workspace_limit(size_t bytes) {
   std::lock_guard<std::mutex> lock(g_mu);

@@ -82,14 +82,18 @@ struct TileRef {
   bool skip;  // a lower-triangle tile of a symmetric single-job launch: nobody touches it
 };
 
+// Tile t of the launch. In the checked build a tile whose job index lies outside the job table, or which
+// does not intersect its product's output (or whose product has no K), is skipped by every role alike and
+// recorded as a range failure.
 __device__ __forceinline__ TileRef tile_at(const GemmLaunch& p, int t, int bn, int tile_m) {
   TileRef r;
   if (p.jobs != nullptr) {
     const GemmTile g = p.tiles[t];
-    r.job = p.jobs + g.job;
+    const bool job_ok = dev_check(g.job >= 0 && g.job < p.njobs, p.status);
+    r.job = p.jobs + (job_ok ? g.job : 0);
     r.tm = g.tm;
     r.tn = g.tn;
-    r.skip = false;
+    r.skip = !job_ok;
   } else {
     // One job: bands of kSingleBand tile rows, walked column by column, so the tiles in flight at
     // once form a near-square block whose A and B panels stay in L2 together.
@@ -102,6 +106,9 @@ __device__ __forceinline__ TileRef tile_at(const GemmLaunch& p, int t, int bn, i
     r.tm = g0 + (u - r.tn * bh);
     r.skip = (p.single.flags & kJobSymmetric) && (r.tn * bn + bn - 1 < r.tm * tile_m);
   }
+  if (!r.skip)
+    r.skip = !dev_check(r.tm >= 0 && r.tn >= 0 && r.tm * tile_m < r.job->M && r.tn * bn < r.job->N && r.job->K > 0,
+                        p.status);
   return r;
 }
 
@@ -396,12 +403,14 @@ __device__ __forceinline__ void gemm_tc_body(const GemmLaunch& p) {
   // first tile's maps while the previous grid finishes.
   if (warp == 0 && lane == 0 && unit < p.ntiles) {
     const TileRef tr0 = tile_at(p, unit, BN, C::kTileM);
-    prefetch_tensormap(&tr0.job->tmA);
-    prefetch_tensormap(&tr0.job->tmB);
-    if (tr0.job->flags & kJobFinal) {
-      if (tr0.job->flags & kJobTmaW) prefetch_tensormap(&tr0.job->tmW);
-    } else {
-      prefetch_tensormap(&tr0.job->tmD);
+    if (!tr0.skip) prefetch_tensormap(&tr0.job->tmA);
+    if (!tr0.skip) {
+      prefetch_tensormap(&tr0.job->tmB);
+      if (tr0.job->flags & kJobFinal) {
+        if (tr0.job->flags & kJobTmaW) prefetch_tensormap(&tr0.job->tmW);
+      } else {
+        prefetch_tensormap(&tr0.job->tmD);
+      }
     }
   }
   griddep_wait();  // the previous phase's outputs are complete and visible before any other global access

@@ -14,7 +14,28 @@ namespace dmuon {
 enum : unsigned {
   kDevTimeout = 1u,    // a bounded mbarrier wait gave up; the launch's results are invalid
   kDevNonfinite = 2u,  // an fp16 store overflowed or was NaN
+  kDevRange = 4u,      // checked build: an index or tile outside its table or matrix was skipped
 };
+
+// Device-side range checks: compiled in with -DDMUON_DEVICE_CHECKS=1 (the checked build,
+// libdmuon_checked.so), left out otherwise. dev_check(ok, status) is ok in the checked build, recording
+// kDevRange in *status (when given) if it is false, so the caller can skip the access; in the regular
+// build it is always true and the condition costs nothing.
+#ifndef DMUON_DEVICE_CHECKS
+#define DMUON_DEVICE_CHECKS 0
+#endif
+#if defined(__CUDACC__)
+__device__ __forceinline__ bool dev_check(bool ok, unsigned* status) {
+#if DMUON_DEVICE_CHECKS
+  if (!ok && status != nullptr) atomicOr(status, kDevRange);
+  return ok;
+#else
+  (void)ok;
+  (void)status;
+  return true;
+#endif
+}
+#endif
 
 // ------------------------------------------------------------------------------------------------
 // Grouped tensor-core GEMM (gemm_tc.cu).
@@ -77,6 +98,7 @@ struct GemmLaunch {
   float alpha, beta, gamma;  // kRecCustom
   float w_alpha, w_beta;     // kJobFinal
   unsigned* status;
+  int njobs;                 // entries of `jobs` (checked build: every tile's job index is tested against it)
 };
 
 // Output tile configurations of the GEMM kernel.
@@ -194,6 +216,8 @@ struct RowLaunch {
   // Device status word for bounded waits. With it the momentum pass streams M and G through a
   // shared-memory ring of bulk copies; without it (the allocation-free entry) it uses vector loads.
   unsigned* status = nullptr;
+  int64_t npartials = 0;  // entries of `partials` (checked build: every partial index is tested against it)
+  unsigned* check_status = nullptr;  // checked build: where range failures are recorded (may be null)
 };
 
 // ------------------------------------------------------------------------------------------------
@@ -218,6 +242,7 @@ struct AdamLaunch {
   const int64_t* chunk_prefix;  // ntensors + 1 exclusive prefix of chunks
   int gdtype;                   // 0 fp32, 1 bf16
   float decay, step_size, inv_bc2, beta1, one_minus_beta1, beta2, one_minus_beta2, eps;
+  unsigned* status;             // checked build: where range failures are recorded
 };
 
 cudaError_t launch_adamw(const AdamLaunch& a, int64_t nchunks, cudaStream_t stream);

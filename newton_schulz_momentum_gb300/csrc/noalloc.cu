@@ -167,6 +167,7 @@ extern "C" int dmuon_momentum_normalize_noalloc(const void* grad, int grad_dtype
   rl.norms_out = norm_out;
   rl.beta = beta;
   rl.eps = eps;
+  rl.npartials = nchunks;
   if ((e = launch_momentum_sumsq(rl, nchunks, stream)) != cudaSuccess ||
       (e = launch_finalize_norms(rl, stream)) != cudaSuccess ||
       (e = launch_normalize_cast(rl, ntiles, stream)) != cudaSuccess)

@@ -221,6 +221,23 @@ __global__ void __launch_bounds__(kSmallThreads, 1) ns_small_kernel(const __grid
   const uint32_t tmem = *tmem_slot;
   const uint32_t my_tmem = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
   griddep_wait();  // the norm pass's results are complete and visible before any global access
+#if DMUON_DEVICE_CHECKS
+  // Checked build: every job's sizes within the kernel's limits, or the launch does nothing.
+  {
+    bool ok = true;
+    for (int j = tid; j < p.njobs; j += kSmallThreads) {
+      const SmallJob& jb = p.jobs[j];
+      ok &= jb.m >= 1 && jb.m <= kSmallMaxM && jb.n >= 1 && jb.n <= kSmallMaxN;
+    }
+    if (!__syncthreads_and(dev_check(ok, p.status))) {
+      tc_fence_before();
+      __syncthreads();
+      tc_fence_after();
+      if (warp == 0) tmem_dealloc(tmem, 512);
+      return;
+    }
+  }
+#endif
 
   uint32_t mma_phase = 0;
   bool bad = false;

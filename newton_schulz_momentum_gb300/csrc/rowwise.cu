@@ -67,8 +67,10 @@ __global__ void __launch_bounds__(kThreads) momentum_sumsq_kernel(const RowLaunc
   __shared__ float red[kThreads / 32];
   const int64_t chunk = p.chunk_base + blockIdx.x;
   const int mi = find_matrix(p.chunk_prefix, p.nmats, chunk);
+  if (!dev_check(mi >= 0 && mi < p.nmats, p.check_status)) return;
   const RowMat mt = p.mats[mi];
   const int64_t local = chunk - p.chunk_prefix[mi];
+  if (!dev_check(local >= 0 && local < mt.part_count && mt.part_begin + local < p.npartials, p.check_status)) return;
   const int64_t numel = mt.rows * mt.cols;
   const int64_t begin = local * kChunkElems;
   const int64_t end = min(begin + static_cast<int64_t>(kChunkElems), numel);
@@ -156,8 +158,12 @@ __global__ void __launch_bounds__(kThreads, 2) momentum_sumsq_bulk_kernel(const 
   volatile int* abort_flag = reinterpret_cast<volatile int*>(full + kRingSlots);
   const int64_t chunk = p.chunk_base + blockIdx.x;
   const int mi = find_matrix(p.chunk_prefix, p.nmats, chunk);
+  if (!dev_check(mi >= 0 && mi < p.nmats, p.check_status)) return;
   const RowMat mt = p.mats[mi];
   const int64_t local = chunk - p.chunk_prefix[mi];
+  if (!dev_check(local >= 0 && local < mt.part_count && mt.part_begin + local < p.npartials && mt.chunk > 0,
+                 p.check_status))
+    return;
   const int64_t numel = mt.rows * mt.cols;
   const int64_t begin = local * mt.chunk;
   const int64_t end = min(begin + mt.chunk, numel);
@@ -258,7 +264,9 @@ __global__ void __launch_bounds__(kThreads, 2) momentum_sumsq_bulk_kernel(const 
 
 __device__ __forceinline__ void finalize_norms_body(const RowLaunch& p) {
   __shared__ double red[kThreads / 32];
+  if (!dev_check(static_cast<int>(blockIdx.x) < p.nmats, p.check_status)) return;
   const RowMat mt = p.mats[blockIdx.x];
+  if (!dev_check(mt.part_begin >= 0 && mt.part_begin + mt.part_count <= p.npartials, p.check_status)) return;
   double s = 0.0;
   for (int k = threadIdx.x; k < mt.part_count; k += kThreads) s += static_cast<double>(p.partials[mt.part_begin + k]);
   const double total = block_sum(s, red);
@@ -291,11 +299,13 @@ __device__ __forceinline__ void normalize_cast_body(const RowLaunch& p) {
   __shared__ float tile[kCastTile][kCastTile + 1];
   const int64_t t = p.tile_base + blockIdx.x;
   const int mi = find_matrix(p.tile_prefix, p.nmats, t);
+  if (!dev_check(mi >= 0 && mi < p.nmats, p.check_status)) return;
   const RowMat mt = p.mats[mi];
   const int64_t local = t - p.tile_prefix[mi];
   const int64_t tiles_c = (mt.cols + kCastTile - 1) / kCastTile;
   const int64_t r0 = (local / tiles_c) * kCastTile;
   const int64_t c0 = (local % tiles_c) * kCastTile;
+  if (!dev_check(local >= 0 && r0 < mt.rows && c0 < mt.cols, p.check_status)) return;
   const float inv = p.inv[mi];
   // 16-byte loads of M need rows of a multiple of 4 floats; 8-byte stores of X need rows of X
   // (ldx halves) of a multiple of 4. Either condition failing falls back to scalar accesses.

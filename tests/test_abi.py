@@ -29,15 +29,28 @@ def header_functions():
 
 
 def test_exports_match_header(L):
+    """Both builds -- libdmuon.so and the checked libdmuon_checked.so -- export exactly what dmuon.h declares."""
     declared = header_functions()
     assert declared, "no declarations found in include/dmuon.h"
     assert sorted(dm.EXPORTS) == declared
     for name in declared:
         assert hasattr(L, name), name
-    out = subprocess.run(["nm", "-D", "--defined-only", dm.LIB_PATH], check=True,
-                         capture_output=True, text=True).stdout
-    exported = sorted(set(re.findall(r" T (dmuon_\w+)", out)))
-    assert exported == declared
+    for path in (dmbuild.LIB, dmbuild.CHECKED_LIB):
+        out = subprocess.run(["nm", "-D", "--defined-only", path], check=True, capture_output=True, text=True).stdout
+        exported = sorted(set(re.findall(r" T (dmuon_\w+)", out)))
+        assert exported == declared, path
+
+
+def test_checked_build_is_marked_and_regular_build_refuses_the_range_selftest(L):
+    """The checked build says so in its version string; the regular build has no device-side range checks
+    and refuses their self-test before touching a device."""
+    checked = ctypes.CDLL(dmbuild.CHECKED_LIB)
+    checked.dmuon_version.restype = ctypes.c_char_p
+    assert b"range checks" in checked.dmuon_version()
+    assert "range checks" not in dm.version()
+    L.dmuon_selftest_range_check.argtypes = [ctypes.c_void_p]
+    rc, msg = _status(L, L.dmuon_selftest_range_check(None))
+    assert rc == dm.ERR_UNSUPPORTED and "range checks" in msg
 
 
 def test_version(L):
