@@ -612,14 +612,18 @@ int build_plan_host(Plan& pl, const PlanKey& key, const std::vector<const void*>
                                          : static_cast<int>(pl.chunk_prefix[i + 1] - pl.chunk_prefix[i]);
     part += r.part_count;
   }
-  // Matrix groups: consecutive runs of gradient bytes in the weights 1 : 3 : 7 : 7 : ... Only the first
-  // group's copy is exposed, so it is small; each later copy has to fit under the previous group's
-  // computation, which takes several times as long as copying the same bytes, so the shares can grow
-  // threefold and then about twofold. Boundary g sits at the cumulative weight of groups 0 .. g-1. One
-  // group for every other plan.
+  // Matrix groups: consecutive runs of gradient bytes in the weights 1 : 2 : 4 : ... : 4 : 2 : 1. Small at
+  // both ends: when the computation outruns the host link, the first group's copy is what stays exposed;
+  // when the link is the slower side, the copies run back to back and what stays exposed is the last
+  // group's computation after the last copy. Boundary g sits at the cumulative weight of groups 0 .. g-1.
+  // One group for every other plan.
   {
     const int ng = (key.kind == kPlanMuon && !pl.small_fused) ? std::max(1, std::min(key.groups, nm)) : 1;
-    auto weight = [](int g) -> int64_t { return g == 0 ? 1 : g == 1 ? 3 : 7; };
+    auto weight = [ng](int g) -> int64_t {
+      if (g == 0 || g == ng - 1) return 1;
+      if (g == 1 || g == ng - 2) return 2;
+      return 4;
+    };
     int64_t wsum = 0;
     for (int g = 0; g < ng; ++g) wsum += weight(g);
     pl.group_begin.assign(1, 0);
@@ -1199,11 +1203,11 @@ int dmuon_muon_step_host(int count, float* const* params, const void* const* gra
     if (groups > kMaxGroups) return fail(DMUON_ERR_INVALID_ARG, "groups must be at most %d", kMaxGroups);
     const size_t esize = grad_dtype == DMUON_BF16 ? 2 : 4;
     if (groups <= 0) {
-      // One group per ~3 GiB of gradients, at most 8: the first group's copy is the part left exposed,
-      // and every group adds one launch per phase.
+      // One group per ~1.75 GiB of gradients, at most 8: fewer groups leave more of the copy or of the
+      // computation exposed at the ends, and every group adds one launch per phase.
       int64_t bytes = 0;
       for (int i = 0; i < count; ++i) bytes += rows[i] * cols[i] * static_cast<int64_t>(esize);
-      const int64_t per_group = int64_t(3) << 30;
+      const int64_t per_group = int64_t(7) << 28;
       groups = static_cast<int>(std::min<int64_t>(8, std::max<int64_t>(1, (bytes + per_group - 1) / per_group)));
     }
     cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
