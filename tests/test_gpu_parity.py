@@ -437,3 +437,33 @@ def test_plan_info_and_launch_timing(dm):
     padded = sum(dm.gram_flops(-(-min(r, c) // 256) * 256, -(-max(r, c) // 256) * 256, dense=True)
                  for r, c in shapes)
     assert tiles > 0 and algo <= flops <= padded
+
+
+@pytest.mark.parametrize("shape", [(1, 1 << 20), (1 << 20, 1), (8, 1 << 18), (3, 100003)])
+@pytest.mark.parametrize("backend", ["gram", "direct"])
+def test_extreme_aspect_ratios(dm, shape, backend):
+    """Very long rows (m up to 8 after orientation, n up to 2^20): the Gram matrix is tiny while X X^T and
+    Q X run over a long K or N; a prime-length side leaves a ragged tail in every tile row."""
+    g = workloads.gaussian(shape, 1.0, 31 + shape[0])
+    got = run_ns(dm, g, dm.YOU, (2,), backend)
+    want = ns64.newton_schulz(g, ns64.YOU, (2,), backend, EPS)
+    assert rel(got, want) <= TOL_NS
+
+
+def test_nonfinite_gradient_is_reported_and_others_unaffected(dm):
+    """An inf in one matrix's gradient makes that matrix's norm and X non-finite: the step reports NONFINITE
+    instead of returning silently. The other matrices of the call are computed as usual."""
+    shapes = [(256, 1024), (300, 700)]
+    W = [workloads.gaussian(s, 0.02, 1700 + i) for i, s in enumerate(shapes)]
+    G = [workloads.gaussian(s, 1.0, 1800 + i) for i, s in enumerate(shapes)]
+    bad = G[0].copy()
+    bad[5, 7] = np.inf
+    Wd = [cuda(w) for w in W]
+    Md = [torch.zeros(s, dtype=torch.float32, device="cuda") for s in shapes]
+    dm.muon_step(Wd, [cuda(bad), cuda(G[1])], Md, lr=0.02, beta=0.95, coeffs=dm.YOU, restarts=(2,), backend="gram")
+    with pytest.raises(dm.DmuonError) as ei:
+        dm.check_status()
+    assert ei.value.status == dm.ERR_NONFINITE
+    ref = muon_ref(W[1], G[1], np.zeros(shapes[1]), 0.02, 0.95, ns64.YOU, (2,), "gram")
+    assert check_update(W[1], Wd[1].cpu().numpy(), ref, 0.02) <= TOL_NS
+    dm.check_status()  # cleared
