@@ -325,10 +325,16 @@ constexpr bool kMirrorQ = false;
 constexpr int64_t kFullSymMaxM = 256;
 int sym_flag(const MatInfo& mi) { return mi.m <= kFullSymMaxM ? 0 : kJobSymmetric; }
 
+// Flags of a product whose operands are symmetric in exact arithmetic (R R, Z R, S Z; A A in the direct
+// form). Mirrored, the stored operands are exactly symmetric and B read K-major (as B^T) is the same
+// product. In full, the stored R and S are symmetric only up to fp16 rounding, so B is read MN-major and
+// the product is the one the step defines: reading it as R R^T, Z R^T and S Z^T instead doubled the error
+// of a 256 x 1024 Gram iteration over what fp16 storage alone causes.
+int sym_product_flags(const MatInfo& mi) { return mi.m <= kFullSymMaxM ? kJobBMnMajor : kJobSymmetric; }
+
 void build_gram_phases(Plan& pl, const std::vector<int>& restarts, int steps, const std::vector<int>& idx,
                        std::vector<std::vector<JobSpec>>& out, std::vector<int>& out_coef) {
   const int nm = static_cast<int>(pl.mats.size());
-  const int s_mirror = kMirrorS ? kJobSymmetric : 0;
   const int q_mirror = kMirrorQ ? kJobSymmetric : 0;
   std::vector<char> is_restart(steps + 1, 0);
   for (int r : restarts)
@@ -395,8 +401,8 @@ void build_gram_phases(Plan& pl, const std::vector<int>& restarts, int steps, co
       std::vector<JobSpec> ph;
       for (int i : idx) {
         const MatInfo& mi = pl.mats[i];
-        ph.push_back(make_job(i, mi.m, mi.m, mi.m, kRecZ, sym_flag(mi) | (fresh ? kJobD2 : 0), mi.R, mi.ldm, mi.R,
-                              mi.ldm, mi.R, mi.ldm, mi.Z, mi.ldm, fresh ? Q[i] : kNone));
+        ph.push_back(make_job(i, mi.m, mi.m, mi.m, kRecZ, sym_product_flags(mi) | (fresh ? kJobD2 : 0), mi.R,
+                              mi.ldm, mi.R, mi.ldm, mi.R, mi.ldm, mi.Z, mi.ldm, fresh ? Q[i] : kNone));
       }
       push(std::move(ph), k);
     }
@@ -410,8 +416,9 @@ void build_gram_phases(Plan& pl, const std::vector<int>& restarts, int steps, co
                                 Q[i], mi.ldm, Q[i], mi.ldm, Qb[i], mi.ldm));
         }
         if (update_r) {  // S = Z R + a R
-          ph.push_back(make_job(i, mi.m, mi.m, mi.m, kRecAxpy, s_mirror & sym_flag(mi), mi.Z, mi.ldm, mi.R, mi.ldm,
-                                mi.R, mi.ldm, mi.S, mi.ldm));
+          const int sf = kMirrorS ? sym_product_flags(mi) : kJobBMnMajor;
+          ph.push_back(make_job(i, mi.m, mi.m, mi.m, kRecAxpy, sf, mi.Z, mi.ldm, mi.R, mi.ldm, mi.R, mi.ldm, mi.S,
+                                mi.ldm));
         }
       }
       push(std::move(ph), k);
@@ -422,8 +429,8 @@ void build_gram_phases(Plan& pl, const std::vector<int>& restarts, int steps, co
       std::vector<JobSpec> ph;
       for (int i : idx) {
         const MatInfo& mi = pl.mats[i];
-        ph.push_back(make_job(i, mi.m, mi.m, mi.m, kRecAxpy, sym_flag(mi), mi.S, mi.ldm, mi.Z, mi.ldm, mi.S, mi.ldm,
-                              mi.R, mi.ldm));
+        ph.push_back(make_job(i, mi.m, mi.m, mi.m, kRecAxpy, sym_product_flags(mi), mi.S, mi.ldm, mi.Z, mi.ldm, mi.S,
+                              mi.ldm, mi.R, mi.ldm));
       }
       push(std::move(ph), k);
     }
@@ -455,8 +462,8 @@ void build_direct_phases(Plan& pl, int steps, const std::vector<int>& idx, std::
       // A = X X^T (in R), B = b A + c A^2 (in Z)
       p1.push_back(make_job(i, mi.m, mi.m, mi.n, kRecPlain, sym_flag(mi), X[i], mi.ldx, X[i], mi.ldx, kNone, 0, mi.R,
                             mi.ldm));
-      p2.push_back(make_job(i, mi.m, mi.m, mi.m, kRecZ, sym_flag(mi), mi.R, mi.ldm, mi.R, mi.ldm, mi.R, mi.ldm, mi.Z,
-                            mi.ldm));
+      p2.push_back(make_job(i, mi.m, mi.m, mi.m, kRecZ, sym_product_flags(mi), mi.R, mi.ldm, mi.R, mi.ldm, mi.R,
+                            mi.ldm, mi.Z, mi.ldm));
       if (k + 1 < steps) {  // X' = B X + a X
         p3.push_back(make_job(i, mi.m, mi.n, mi.m, kRecAxpy, kJobBMnMajor, mi.Z, mi.ldm, X[i], mi.ldx, X[i], mi.ldx,
                               Xb[i], mi.ldx));

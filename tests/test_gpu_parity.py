@@ -327,8 +327,8 @@ def test_small_matrix_set_one_grouped_step(dm):
     normalised singular values lie in [0.044, 0.133], where the composition of the printed POLAR_EXPRESS
     polynomials runs from 1.02 up to 2.5e5 with slopes up to 4e7, so fp16 rounding of the intermediates is
     amplified far more than with YOU (range 0.98 .. 1.03, slopes below 12). Any fp16 iteration lands near
-    5e-2 here: a NumPy emulation of the same fp16-operand, fp32-accumulation Gram iteration gives 5.2e-2
-    on this shape, and the kernel measures 4.9e-2."""
+    5e-2 here: the fp16 error model (oracle/fp16_model.py) gives 4.7e-2 to 5.6e-2 on these matrices, and
+    tests/test_gpu_error_floor.py holds the kernel to that floor matrix by matrix."""
     shapes = workloads.small_set_shapes()
     G = [workloads.gaussian(s, 1e-3, 1000 + i) for i, s in enumerate(shapes)]
     W = [workloads.gaussian(s, 0.02, 5000 + i) for i, s in enumerate(shapes)]
