@@ -137,8 +137,9 @@ DMUON_API int dmuon_muon_step(int count, float* const* params, const void* const
  * ranks, not from the host; this is the single-GPU form of "gradients in, update out".) Equivalent to
  * copying every grads_host[i] into grads[i] and then calling dmuon_muon_step, with identical results,
  * but the copies overlap the computation: the matrices are taken in `groups` consecutive groups by
- * gradient bytes, in the weights 1 : 2 : 4 : ... : 4 : 2 : 1 (small at both ends: with a fast host link the
- * first group's copy is what stays exposed, with a slow one the last group's computation);
+ * gradient bytes, their weights rising 1 : 2 : 3 from the start and falling by a factor 0.85 per group
+ * towards the end (with a fast host link the first group's copy is what stays exposed, with a slow one
+ * the computation still queued after the last copy);
  * group g's copies run on the library's copy stream while earlier groups compute on
  * cuda_stream, and group g's momentum pass waits only for its own copies. Each group runs its row-wise
  * passes and Newton-Schulz phases as grouped launches of its own. With many small matrices (64 or more
@@ -153,8 +154,8 @@ DMUON_API int dmuon_muon_step(int count, float* const* params, const void* const
  *               overlap. The caller keeps them unchanged until cuda_stream has passed this call.
  *   grads       host array of `count` device buffers (as in dmuon_muon_step) receiving the gradients;
  *               they are overwritten.
- *   groups      pipeline depth in [1, 64]; <= 0 lets the library choose (one group per ~1.75 GiB of
- *               gradients, at most 8). More groups than matrices gives one matrix per group.
+ *   groups      pipeline depth in [1, 64]; <= 0 lets the library choose (one group per ~1 GiB of
+ *               gradients, at most 16). More groups than matrices gives one matrix per group.
  *   Other arguments as in dmuon_muon_step.
  * Ordering: the copies start after all work enqueued on cuda_stream before the call and after the
  * previous dmuon_muon_step_host call on this device has read its gradients; all of the call's work,

@@ -619,17 +619,19 @@ int build_plan_host(Plan& pl, const PlanKey& key, const std::vector<const void*>
                                          : static_cast<int>(pl.chunk_prefix[i + 1] - pl.chunk_prefix[i]);
     part += r.part_count;
   }
-  // Matrix groups: consecutive runs of gradient bytes in the weights 1 : 2 : 4 : ... : 4 : 2 : 1. Small at
-  // both ends: when the computation outruns the host link, the first group's copy is what stays exposed;
-  // when the link is the slower side, the copies run back to back and what stays exposed is the last
-  // group's computation after the last copy. Boundary g sits at the cumulative weight of groups 0 .. g-1.
-  // One group for every other plan.
+  // Matrix groups: consecutive runs of gradient bytes. When the computation outruns the host link, the
+  // first group's copy is what stays exposed, so the weights rise 1 : 2 : 3 from the start. When the link is
+  // the slower side, the copies run back to back and what stays exposed is the computation still queued
+  // after the last copy: the weights fall towards the end by a factor 0.85 per group (to 1.13 for the
+  // last), so that each group's computation fits under the next group's copy down to a link at ~0.85 of
+  // the computation's rate, and the last group is small. Weight of group g = min(ramp, fall) in hundredths;
+  // boundary g sits at the cumulative weight of groups 0 .. g-1. One group for every other plan.
   {
     const int ng = (key.kind == kPlanMuon && !pl.small_fused) ? std::max(1, std::min(key.groups, nm)) : 1;
     auto weight = [ng](int g) -> int64_t {
-      if (g == 0 || g == ng - 1) return 1;
-      if (g == 1 || g == ng - 2) return 2;
-      return 4;
+      const int64_t ramp = std::min<int64_t>(100 * (g + 1), 300);
+      const int64_t fall = static_cast<int64_t>(std::min(300.0, 113.0 * std::pow(1.0 / 0.85, ng - 1 - g)));
+      return std::min(ramp, fall);
     };
     int64_t wsum = 0;
     for (int g = 0; g < ng; ++g) wsum += weight(g);
@@ -1210,12 +1212,13 @@ int dmuon_muon_step_host(int count, float* const* params, const void* const* gra
     if (groups > kMaxGroups) return fail(DMUON_ERR_INVALID_ARG, "groups must be at most %d", kMaxGroups);
     const size_t esize = grad_dtype == DMUON_BF16 ? 2 : 4;
     if (groups <= 0) {
-      // One group per ~1.75 GiB of gradients, at most 8: fewer groups leave more of the copy or of the
-      // computation exposed at the ends, and every group adds one launch per phase.
+      // One group per ~1 GiB of gradients, at most 16: fewer groups leave more of the copy or of the
+      // computation exposed at the ends, and every group adds one launch per phase (measured: twelve
+      // groups of the 8B set add under 2% to the GEMM time).
       int64_t bytes = 0;
       for (int i = 0; i < count; ++i) bytes += rows[i] * cols[i] * static_cast<int64_t>(esize);
-      const int64_t per_group = int64_t(7) << 28;
-      groups = static_cast<int>(std::min<int64_t>(8, std::max<int64_t>(1, (bytes + per_group - 1) / per_group)));
+      const int64_t per_group = int64_t(1) << 30;
+      groups = static_cast<int>(std::min<int64_t>(16, std::max<int64_t>(1, (bytes + per_group - 1) / per_group)));
     }
     cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
     std::lock_guard<std::mutex> lock(g_mu);
