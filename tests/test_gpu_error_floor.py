@@ -104,3 +104,23 @@ def test_top_tenth_closed_form_at_the_fp16_floor(dm):
     got = xd.cpu().numpy()
     assert_at_floor(lambda want: rel(got, want), g.astype(np.float64), ns64.POLAR_EXPRESS, (2,), "gram",
                     "2048x8192 top tenth")
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("backend", ["gram", "direct"])
+def test_llama_shapes_at_the_fp16_floor(dm, backend):
+    """One Muon step over the four Llama-3-8B projection shapes (q/o 4096 x 4096, k/v 1024 x 4096, gate/up
+    14336 x 4096, down 4096 x 14336), bf16 gradients N(0, 1e-3^2), momentum from zero, POLAR_EXPRESS: the
+    grouped launches with 256 x 256 CTA-pair tiles and mirrored symmetric products that the 8B step runs."""
+    shapes = [(4096, 4096), (1024, 4096), (14336, 4096), (4096, 14336)]
+    G = [workloads.round_to_bf16(workloads.gaussian(s, 1e-3, 700 + i))[0] for i, s in enumerate(shapes)]
+    W = [workloads.gaussian(s, 0.02, 800 + i) for i, s in enumerate(shapes)]
+    Wd = [torch.from_numpy(w).cuda() for w in W]
+    Gd = [torch.from_numpy(g).cuda().to(torch.bfloat16) for g in G]
+    Md = [torch.zeros(s, dtype=torch.float32, device="cuda") for s in shapes]
+    dm.muon_step(Wd, Gd, Md, lr=0.02, beta=0.95, coeffs=dm.POLAR_EXPRESS, restarts=(2,), backend=backend)
+    dm.check_status()
+    for k, s in enumerate(shapes):
+        upd = (W[k].astype(np.float64) - Wd[k].cpu().numpy().astype(np.float64)) / 0.02
+        # momentum from zero: M = G (the bf16 values, exact in fp32)
+        assert_at_floor(lambda want: rel(upd, want), G[k], ns64.POLAR_EXPRESS, (2,), backend, f"{s} {backend}")
