@@ -52,6 +52,7 @@ EXPORTS = (
     "dmuon_release_workspace", "dmuon_timing_enable", "dmuon_timing_read", "dmuon_momentum_normalize_noalloc",
     "dmuon_assign_owners", "dmuon_adamw_step", "dmuon_ns_tp", "dmuon_muon_step_host",
     "dmuon_timing_read_launches", "dmuon_plan_info", "dmuon_selftest_bounded_wait", "dmuon_selftest_range_check",
+    "dmuon_set_graph_replay",
 )
 COST_MODELS = {"elements": 0, "gram_flops": 1, "direct_flops": 2}
 NOALLOC_MAX_ELEMS = 268435456
@@ -100,6 +101,7 @@ def lib():
     L.dmuon_workspace_size.argtypes = [i32, _c_i64p, _c_i64p, i32, ctypes.POINTER(ctypes.c_size_t)]
     L.dmuon_momentum_normalize_noalloc.argtypes = [vp, i32, vp, i64, i64, vp, vp, f32, f32, vp]
     L.dmuon_timing_enable.argtypes = [i32]
+    L.dmuon_set_graph_replay.argtypes = [i32]
     f64 = ctypes.c_double
     L.dmuon_adamw_step.argtypes = [i32, _c_vpp, _c_vpp, i32, _c_vpp, _c_vpp, _c_i64p, f64, f64, f64, f64, f64, i32, vp]
     L.dmuon_assign_owners.argtypes = [i32, _c_i64p, _c_i64p, _c_ip, i32, i32, _c_ip, ctypes.POINTER(ctypes.c_double)]
@@ -365,6 +367,12 @@ def workspace_size(shapes, backend="gram"):
     out = ctypes.c_size_t(0)
     _check(lib().dmuon_workspace_size(n, rows, cols, _backend(backend), ctypes.byref(out)))
     return out.value
+
+
+def set_graph_replay(on=True):
+    """Graph replay of repeated calls (on by default): the second consecutive call with the same plan and
+    arguments is captured as a CUDA graph and later such calls launch it; off launches every call directly."""
+    _check(lib().dmuon_set_graph_replay(1 if on else 0))
 
 
 def timing_enable(on=True):

@@ -171,6 +171,19 @@ struct AdamPlan {
   bool bound = false;
 };
 
+// What a captured run of the cached plan baked in besides the plan itself.
+struct GraphKey {
+  bool valid = false;
+  uint64_t plan_serial = 0;
+  std::vector<float> coeffs;
+  float lr = 0.f, beta = 0.f, eps = 0.f;
+  float* norms_out = nullptr;
+  bool operator==(const GraphKey& o) const {
+    return valid && o.valid && plan_serial == o.plan_serial && coeffs == o.coeffs && lr == o.lr &&
+           beta == o.beta && eps == o.eps && norms_out == o.norms_out;
+  }
+};
+
 struct DeviceState {
   bool init = false;
   int sms = 0;
@@ -178,6 +191,12 @@ struct DeviceState {
   char* arena = nullptr;
   size_t arena_bytes = 0;
   Plan plan;
+  uint64_t plan_serial = 0;  // bumped whenever the cached plan or its workspace changes
+  // Graph replay of the cached plan: `graph` runs the launches run_plan issues for `graph_key`; `last_key`
+  // is the previous call's, so that a run is captured the second time the same arguments come.
+  cudaStream_t capture_stream = nullptr;
+  cudaGraphExec_t graph = nullptr;
+  GraphKey graph_key, last_key;
   AdamPlan adam;
   // Host-gradient pipeline (dmuon_muon_step_host): the copy stream, an event marking the caller's stream
   // at entry, and per group the "gradients arrived" and "gradients read by the momentum pass" events.
@@ -195,6 +214,7 @@ struct DeviceState {
 
 std::mutex g_mu;
 constexpr int kMaxDevices = 64;
+bool g_graphs = true;  // dmuon_set_graph_replay
 
 // Opt-in event timing (dmuon_timing_enable / dmuon_timing_read).
 struct TimedLaunch {
@@ -936,6 +956,7 @@ int ensure_plan(DeviceState& ds, const PlanKey& key, const std::vector<const voi
   if (rebuilt) *rebuilt = false;
   if (ds.plan.bound && ds.plan.key == key) return DMUON_OK;
   if (rebuilt) *rebuilt = true;
+  ++ds.plan_serial;
   ds.plan = Plan();
   int st = build_plan_host(ds.plan, key, G, Mom, W, xout, gemm_max_units(kTilePair256, ds.sms));
   if (st != DMUON_OK) return st;
@@ -944,7 +965,43 @@ int ensure_plan(DeviceState& ds, const PlanKey& key, const std::vector<const voi
   return st;
 }
 
-// Shared body of the plan-based entry points that take device buffers.
+void drop_graph(DeviceState& ds) {
+  if (ds.graph) cudaGraphExecDestroy(ds.graph);
+  ds.graph = nullptr;
+  ds.graph_key = GraphKey();
+}
+
+// Capture one run of the cached plan on the library's private stream and instantiate it. On any failure
+// the capture is abandoned, the error cleared, and false returned: the caller launches directly instead.
+bool capture_plan(DeviceState& ds, const float* coeffs, float lr, float beta, float eps, float* norms_out) {
+  drop_graph(ds);
+  if (!ds.capture_stream && cudaStreamCreateWithFlags(&ds.capture_stream, cudaStreamNonBlocking) != cudaSuccess) {
+    ds.capture_stream = nullptr;
+    cudaGetLastError();
+    return false;
+  }
+  if (cudaStreamBeginCapture(ds.capture_stream, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  const int st = run_plan(ds, ds.plan, coeffs, lr, beta, eps, norms_out, ds.capture_stream);
+  cudaGraph_t g = nullptr;
+  const cudaError_t e = cudaStreamEndCapture(ds.capture_stream, &g);
+  bool ok = st == DMUON_OK && e == cudaSuccess && g != nullptr &&
+            cudaGraphInstantiate(&ds.graph, g, 0) == cudaSuccess;
+  if (g) cudaGraphDestroy(g);
+  if (!ok) {
+    ds.graph = nullptr;
+    cudaGetLastError();
+  }
+  return ok;
+}
+
+// Shared body of the plan-based entry points that take device buffers. With graph replay on (the default),
+// no per-launch timing and a caller's stream that is not itself being captured, the second consecutive call with the same plan and the same arguments captures
+// the plan's launches as a CUDA graph, and every further such call launches that graph on the caller's
+// stream: the same kernels with the same arguments, so the same results bit for bit, with the per-launch
+// issue cost of the chain of small dependent launches taken off. Any other call launches directly.
 int plan_and_run(const PlanKey& key, const std::vector<const void*>& G, const std::vector<float*>& Mom,
                  const std::vector<float*>& W, const std::vector<void*>& xout, const float* coeffs, float lr,
                  float beta, float eps, float* norms_out, cudaStream_t stream) {
@@ -954,7 +1011,29 @@ int plan_and_run(const PlanKey& key, const std::vector<const void*>& G, const st
   if (st != DMUON_OK) return st;
   st = ensure_plan(*ds, key, G, Mom, W, xout, stream);
   if (st != DMUON_OK) return st;
-  return run_plan(*ds, ds->plan, coeffs, lr, beta, eps, norms_out, stream);
+  // A stream the caller is capturing gets the launches themselves, so that they become part of the
+  // caller's graph.
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) {
+    cudaGetLastError();
+    cs = cudaStreamCaptureStatusActive;
+  }
+  if (!g_graphs || g_timing || cs != cudaStreamCaptureStatusNone)
+    return run_plan(*ds, ds->plan, coeffs, lr, beta, eps, norms_out, stream);
+  GraphKey gk;
+  gk.valid = true;
+  gk.plan_serial = ds->plan_serial;
+  gk.coeffs.assign(coeffs, coeffs + 3 * ds->plan.key.steps);
+  gk.lr = lr, gk.beta = beta, gk.eps = eps, gk.norms_out = norms_out;
+  if (!(ds->graph && ds->graph_key == gk)) {
+    const bool repeat = ds->last_key == gk;
+    ds->last_key = gk;
+    if (!repeat || !capture_plan(*ds, coeffs, lr, beta, eps, norms_out))
+      return run_plan(*ds, ds->plan, coeffs, lr, beta, eps, norms_out, stream);
+    ds->graph_key = gk;
+  }
+  DM_CUDA(cudaGraphLaunch(ds->graph, stream), "cudaGraphLaunch of the cached plan");
+  return DMUON_OK;
 }
 
 // The copy stream and at least `n` pairs of group events of the host-gradient pipeline.
@@ -1481,6 +1560,12 @@ int dmuon_adamw_step(int count, float* const* params, const void* const* grads, 
   }
 }
 
+int dmuon_set_graph_replay(int on) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  g_graphs = on != 0;
+  return DMUON_OK;
+}
+
 int dmuon_timing_enable(int on) {
   std::lock_guard<std::mutex> lock(g_mu);
   for (auto& t : g_timed) {
@@ -1643,6 +1728,9 @@ int dmuon_release_workspace(void) {
   ds.arena = nullptr;
   ds.arena_bytes = 0;
   ds.plan = Plan();
+  ++ds.plan_serial;
+  drop_graph(ds);
+  ds.last_key = GraphKey();
   if (ds.adam.buf) {
     DM_CUDA(cudaDeviceSynchronize(), "cudaDeviceSynchronize");
     DM_CUDA(cudaFree(ds.adam.buf), "cudaFree(AdamW table)");
