@@ -529,12 +529,15 @@ int64_t count_tiles(const std::vector<JobSpec>& ph, int tile) {
 
 // A launch whose 256 x 256 pair tiles cannot fill the CTA pairs (a phase of a single matrix, or of a
 // few, of moderate size) runs on 128 x 128 single-CTA tiles instead: about four times the work units,
-// and half of a pair tile's epilogue per warp, for phases that would otherwise leave most SMs idle.
+// and half of a pair tile's epilogue per warp, for phases that would otherwise leave most SMs idle. When
+// even those would occupy fewer than half of the SMs (`pair_units` is half the SM count), the tiles are
+// halved again to 128 x 64: twice the work units, each with half the MMAs and one epilogue chunk per warp.
 int launch_tile(const std::vector<JobSpec>& ph, int pair_units) {
   int max_m = 0, max_n = 0;
   for (const JobSpec& j : ph) max_m = std::max(max_m, j.M), max_n = std::max(max_n, j.N);
-  const int tile = pick_tile(max_m, max_n);
-  if (tile == kTilePair256 && count_tiles(ph, kTilePair256) < pair_units) return kTileSingle128;
+  int tile = pick_tile(max_m, max_n);
+  if (tile == kTilePair256 && count_tiles(ph, kTilePair256) < pair_units) tile = kTileSingle128;
+  if (tile == kTileSingle128 && count_tiles(ph, kTileSingle128) < pair_units) tile = kTileSingle64;
   return tile;
 }
 

@@ -7,7 +7,7 @@
 // jobs (one job = one product on one matrix), so all matrices a rank owns advance one phase per
 // launch.
 //
-// CTA layout (192 threads, or 320 for 128 x 128 tiles; one persistent CTA per SM):
+// CTA layout (192 threads, or 320 for 128 x 128 and 128 x 64 tiles; one persistent CTA per SM):
 //   warp 0      TMA producer: one thread streams 128 x 64 A tiles and BN x 64 B tiles into a
 //               STAGES-deep ring of 128-byte-swizzled shared memory buffers.
 //   warp 1      allocates tensor memory; one thread issues tcgen05.mma (M=128, N=BN, K=16) into one
@@ -15,13 +15,14 @@
 //   warps 2-5   epilogue: tcgen05.ld the accumulator (warp w reads TMEM lanes 32*(w%4)..+31, i.e.
 //               one output row per thread), combine with the step's scalars and an optional fp16
 //               addend, store fp16 (mirrored for symmetric outputs) or update the fp32 weights.
-//               128 x 128 tiles run only in launches too small to fill the machine, where the
-//               epilogue is the critical path: warps 2-9, two per lane quarter, each half the columns.
+//               128 x 128 and 128 x 64 tiles run only in launches too small to fill the machine,
+//               where the epilogue is the critical path: warps 2-9, two per lane quarter, each half the
+//               columns.
 // The accumulator is double-buffered so a tile's epilogue overlaps the next tile's main loop.
-// Three tile configurations: 256 x 256 tiles on CTA pairs (a cluster of two; tcgen05.mma.cta_group::2,
-// each CTA holding half of A and half of B per stage), 128 x 256 and 128 x 128 on single CTAs; the
-// planner takes the pair tiles unless a launch could not fill the pairs or its products are at most 128
-// wide. Launches are programmatic: a grid lets the next phase be scheduled at entry, and sets up its
+// Four tile configurations: 256 x 256 tiles on CTA pairs (a cluster of two; tcgen05.mma.cta_group::2,
+// each CTA holding half of A and half of B per stage), 128 x 256, 128 x 128 and 128 x 64 on single CTAs;
+// the planner takes the pair tiles unless a launch could not fill the pairs or its products are at most
+// 128 wide, and halves 128 x 128 tiles to 128 x 64 when they would fill under half of the SMs. Launches are programmatic: a grid lets the next phase be scheduled at entry, and sets up its
 // barriers and tensor memory (and prefetches its first tensor maps) before waiting for the previous
 // grid.
 //
@@ -49,11 +50,11 @@ struct Cfg {
   static constexpr int kBBytes = kBRows * kBK * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
   // Epilogue warps: one per TMEM lane quarter, or two (each draining half of the tile's columns) for the
-  // 128 x 128 tiles of launches too small to fill the machine, whose epilogue is their critical path;
-  // those also double-buffer their staging (a chunk is written while the previous one's stores read the
-  // other buffer) and keep five ring stages to make room.
-  static constexpr bool kSmallTile = BN == 128 && CG == 1;
-  static constexpr int kStages = kSmallTile ? 5 : (kStageBytes <= 32768) ? 6 : 4;
+  // 128 x 128 and 128 x 64 tiles of launches too small to fill the machine, whose epilogue is their
+  // critical path; those also double-buffer their staging (a chunk is written while the previous one's
+  // stores read the other buffer) and keep fewer ring stages to make room.
+  static constexpr bool kSmallTile = BN <= 128 && CG == 1;
+  static constexpr int kStages = kSmallTile ? (BN == 64 ? 6 : 5) : (kStageBytes <= 32768) ? 6 : 4;
   static constexpr int kTmemCols = 2 * BN;  // two accumulators of BN fp32 columns
   static constexpr int kEpiWarps = kSmallTile ? 8 : 4;
   static constexpr int kEpiBufs = kSmallTile ? 2 : 1;  // 4 KB staging buffers per epilogue warp
@@ -779,6 +780,12 @@ cudaError_t launch_gemm(const GemmLaunch& p, int tile, int units, cudaStream_t s
                                Cfg<256, 1>::kSmemBytes);
       if (e != cudaSuccess) return e;
       e = launch_programmatic(gemm_tc_kernel<256>, units, Cfg<256, 1>::kThreads, Cfg<256, 1>::kSmemBytes, p, stream);
+      break;
+    case kTileSingle64:
+      e = cudaFuncSetAttribute(gemm_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               Cfg<64, 1>::kSmemBytes);
+      if (e != cudaSuccess) return e;
+      e = launch_programmatic(gemm_tc_kernel<64>, units, Cfg<64, 1>::kThreads, Cfg<64, 1>::kSmemBytes, p, stream);
       break;
     default:
       e = cudaFuncSetAttribute(gemm_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,

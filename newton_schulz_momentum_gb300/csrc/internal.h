@@ -106,9 +106,10 @@ enum TileConfig : int {
   kTileSingle128 = 0,  // one CTA, 128 x 128 tile (products with N <= 128)
   kTileSingle256 = 1,  // one CTA, 128 x 256 tile
   kTilePair256 = 2,    // a CTA pair (cluster of 2, tcgen05 cta_group::2), 256 x 256 tile
+  kTileSingle64 = 3,   // one CTA, 128 x 64 tile (launches whose 128 x 128 tiles would fill under half the SMs)
 };
 inline int tile_rows(int tile) { return tile == kTilePair256 ? 256 : 128; }
-inline int tile_cols(int tile) { return tile == kTileSingle128 ? 128 : 256; }
+inline int tile_cols(int tile) { return tile == kTileSingle128 ? 128 : tile == kTileSingle64 ? 64 : 256; }
 inline int tile_ctas(int tile) { return tile == kTilePair256 ? 2 : 1; }
 
 // Largest number of persistent workers of a tile configuration that fit on the device at once.
