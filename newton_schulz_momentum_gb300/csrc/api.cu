@@ -535,8 +535,15 @@ int64_t count_tiles(const std::vector<JobSpec>& ph, int tile) {
 int launch_tile(const std::vector<JobSpec>& ph, int pair_units) {
   int max_m = 0, max_n = 0;
   for (const JobSpec& j : ph) max_m = std::max(max_m, j.M), max_n = std::max(max_n, j.N);
+  int max_k = 0;
+  for (const JobSpec& j : ph) max_k = std::max(max_k, j.K);
   int tile = pick_tile(max_m, max_n);
-  if (tile == kTilePair256 && count_tiles(ph, kTilePair256) < pair_units) tile = kTileSingle128;
+  // Short contractions (K <= 2048: the m x m products of matrices up to 2048 wide) keep the pair tiles down
+  // to half the pairs (measured on one GB300: the full 2048 x 2048 products of a 2048 x 8192 matrix, 64
+  // pair tiles, 31.7 -> 27.6 us per launch on pairs; the symmetric ones, 36 pair tiles, were slower on
+  // pairs, 20.4 -> 26.5 us, so the floor stays above them).
+  const int64_t pair_floor = max_k <= 2048 ? pair_units / 2 : pair_units;
+  if (tile == kTilePair256 && count_tiles(ph, kTilePair256) < pair_floor) tile = kTileSingle128;
   if (tile == kTileSingle128 && count_tiles(ph, kTileSingle128) < pair_units) tile = kTileSingle64;
   return tile;
 }
