@@ -439,6 +439,22 @@ def test_plan_info_and_launch_timing(dm):
     assert tiles > 0 and algo <= flops <= padded
 
 
+def test_small_launches_take_128x64_tiles(dm):
+    """A lone 256 x 1024 matrix: every GEMM launch would fill under half the SMs with 128 x 128 tiles, so
+    each takes 128 x 64 tiles. 17 launches (Gram, restart [2]); the products of m <= 256 are computed in
+    full: 8 tiles for each 256 x 256 product, 16 for the launch holding two of them, 32 for each Q X
+    (256 x 1024). Executed flops: 2 * 128 * 64 * K per tile (K = 1024 for X X^T, 256 otherwise)."""
+    W = [cuda(workloads.gaussian((256, 1024), 0.02, 70))]
+    G = [cuda(workloads.gaussian((256, 1024), 1.0, 71))]
+    M = [torch.zeros((256, 1024), dtype=torch.float32, device="cuda")]
+    dm.muon_step(W, G, M, lr=0.02, beta=0.95, coeffs=dm.YOU, restarts=(2,), backend="gram")
+    dm.check_status()
+    flops, tiles, gemm_launches = dm.plan_info()
+    assert gemm_launches == 17
+    assert tiles == 14 * 8 + 16 + 2 * 32
+    assert flops == 2.0 * 128 * 64 * (2 * 8 * 1024 + (12 * 8 + 16 + 2 * 32) * 256)
+
+
 @pytest.mark.parametrize("shape", [(1, 1 << 20), (1 << 20, 1), (8, 1 << 18), (3, 100003)])
 @pytest.mark.parametrize("backend", ["gram", "direct"])
 def test_extreme_aspect_ratios(dm, shape, backend):
