@@ -510,15 +510,17 @@ __device__ __forceinline__ void gemm_tc_body(const GemmLaunch& p) {
         for (int kb = 0; kb < nkb; ++kb) {
           // Full barriers are checked three ring slots at a time (this slot and the next two of the tile):
           // the probes overlap one another, and the MMA issue is interrupted by a barrier check once per
-          // twelve MMAs instead of once per four.
-          if (kb % 3 == 0) {
+          // twelve MMAs instead of once per four. Short contractions (at most 8 slots) check slot by slot:
+          // there the first MMAs issue as soon as their own slot lands rather than two slots later.
+          const bool per_slot = nkb <= 8;
+          if (per_slot || kb % 3 == 0) {
             const int s1 = stage + 1 == C::kStages ? 0 : stage + 1;
             const uint32_t p1 = stage + 1 == C::kStages ? phase ^ 1u : phase;
             const int s2 = s1 + 1 == C::kStages ? 0 : s1 + 1;
             const uint32_t p2 = s1 + 1 == C::kStages ? p1 ^ 1u : p1;
             const bool r0 = mbar_try_wait(&full[stage], phase);
-            const bool r1 = kb + 1 >= nkb || mbar_try_wait(&full[s1], p1);
-            const bool r2 = kb + 2 >= nkb || mbar_try_wait(&full[s2], p2);
+            const bool r1 = per_slot || kb + 1 >= nkb || mbar_try_wait(&full[s1], p1);
+            const bool r2 = per_slot || kb + 2 >= nkb || mbar_try_wait(&full[s2], p2);
             if (!(r0 && r1 && r2)) {
               if ((!r0 && !wait_bounded(&full[stage], phase, abort_flag, p.status, kWaitLimitNs, true)) ||
                   (!r1 && !wait_bounded(&full[s1], p1, abort_flag, p.status, kWaitLimitNs, true)) ||
